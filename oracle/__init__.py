@@ -1,0 +1,227 @@
+"""CPU oracle for the AdaLN ``norm_out`` operator (test infrastructure).
+
+The arithmetic lives in ``adaln_oracle.c`` (plain C, fp64 with the operator's
+rounding points, IEEE as written, no FMA contraction).  This module only
+compiles it with gcc and marshals numpy arrays into it.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg use this
+package; the CUDA library never imports it, and it imports nothing from the
+CUDA library.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "adaln_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liboracle.so`` next to its source."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        F = ctypes.c_float
+        Dd = ctypes.c_double
+        Lg = ctypes.c_long
+        sig = {
+            "oracle_silu_bf16": [P, P, Lg],
+            "oracle_dsilu_f64": [P, P, Lg],
+            "oracle_proj_fwd": [P, P, P, P, I, I],
+            "oracle_proj_fwd_f64": [P, P, P, P, I, I],
+            "oracle_out_fwd": [P, P, F, P, P, P, I, I, I],
+            "oracle_out_fwd_f64": [P, P, P, Dd, P, I, I, I],
+            "oracle_out_bwd": [P, P, P, F, P, P, I, I, I],
+            "oracle_out_bwd_f64": [P, P, P, Dd, P, P, P, I, I, I],
+            "oracle_token_sum_f64": [P, P, I, I, I],
+            "oracle_token_tree_f32": [P, P, I, I, I],
+            "oracle_bwd_products_f32": [P, P, P, P, P, I, I, I],
+            "oracle_proj_bwd": [P, P, P, P, P, P, I, I],
+            "oracle_proj_bwd_f64": [P, P, P, P, P, P, I, I],
+            "oracle_wgrad_seq_f32": [P, P, P, P, I, I, I],
+            "oracle_bf16_from_f64": [P, P, Lg],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = None
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+EPS = np.float32(1e-6)
+
+
+# --- projection -----------------------------------------------------------
+
+def silu_bf16(t):
+    t = _c(t, np.uint16)
+    u = np.empty_like(t)
+    _load().oracle_silu_bf16(_p(t), _p(u), t.size)
+    return u
+
+
+def dsilu_f64(t):
+    t = _c(t, np.float64)
+    o = np.empty_like(t)
+    _load().oracle_dsilu_f64(_p(t), _p(o), t.size)
+    return o
+
+
+def proj_fwd(temb, W, b):
+    """emb[B, 2D] (bf16 bits) = bf16(bf16(silu(temb)) @ W^T + b)."""
+    temb, W, b = _c(temb, np.uint16), _c(W, np.uint16), _c(b, np.uint16)
+    B, D = temb.shape
+    assert W.shape == (2 * D, D) and b.shape == (2 * D,)
+    emb = np.empty((B, 2 * D), dtype=np.uint16)
+    _load().oracle_proj_fwd(_p(temb), _p(W), _p(b), _p(emb), B, D)
+    return emb
+
+
+def proj_fwd_f64(temb, W, b):
+    temb, W, b = _c(temb, np.float64), _c(W, np.float64), _c(b, np.float64)
+    B, D = temb.shape
+    emb = np.empty((B, 2 * D), dtype=np.float64)
+    _load().oracle_proj_fwd_f64(_p(temb), _p(W), _p(b), _p(emb), B, D)
+    return emb
+
+
+# --- LayerNorm + modulation -------------------------------------------------
+
+def out_fwd(x, emb, eps=EPS):
+    """(out bf16 bits [B,S,D], mean fp32 [B,S], rstd fp32 [B,S])."""
+    x, emb = _c(x, np.uint16), _c(emb, np.uint16)
+    B, S, D = x.shape
+    assert emb.shape == (B, 2 * D)
+    out = np.empty_like(x)
+    mean = np.empty((B, S), dtype=np.float32)
+    rstd = np.empty((B, S), dtype=np.float32)
+    _load().oracle_out_fwd(_p(x), _p(emb), float(eps), _p(out), _p(mean), _p(rstd), B, S, D)
+    return out, mean, rstd
+
+
+def out_fwd_f64(x, scale, shift, eps=1e-6):
+    x, scale, shift = _c(x, np.float64), _c(scale, np.float64), _c(shift, np.float64)
+    B, S, D = x.shape
+    out = np.empty_like(x)
+    _load().oracle_out_fwd_f64(_p(x), _p(scale), _p(shift), float(eps), _p(out), B, S, D)
+    return out
+
+
+def out_bwd(dy, x, emb, eps=EPS):
+    """(dx bf16 bits [B,S,D], d_emb fp32 [B,2D] = [d_scale | d_shift])."""
+    dy, x, emb = _c(dy, np.uint16), _c(x, np.uint16), _c(emb, np.uint16)
+    B, S, D = x.shape
+    dx = np.empty_like(x)
+    d_emb = np.empty((B, 2 * D), dtype=np.float32)
+    _load().oracle_out_bwd(_p(dy), _p(x), _p(emb), float(eps), _p(dx), _p(d_emb), B, S, D)
+    return dx, d_emb
+
+
+def out_bwd_f64(dy, x, scale, eps=1e-6):
+    dy, x, scale = _c(dy, np.float64), _c(x, np.float64), _c(scale, np.float64)
+    B, S, D = x.shape
+    dx = np.empty_like(x)
+    ds = np.empty((B, D), dtype=np.float64)
+    dh = np.empty((B, D), dtype=np.float64)
+    _load().oracle_out_bwd_f64(_p(dy), _p(x), _p(scale), float(eps), _p(dx), _p(ds), _p(dh), B, S, D)
+    return dx, ds, dh
+
+
+# --- token sums -----------------------------------------------------------
+
+def token_sum_f64(a):
+    a = _c(a, np.float32)
+    B, S, H = a.shape
+    out = np.empty((B, H), dtype=np.float64)
+    _load().oracle_token_sum_f64(_p(a), _p(out), B, S, H)
+    return out
+
+
+def token_tree_f32(a):
+    a = _c(a, np.float32)
+    B, S, H = a.shape
+    assert S >= 1
+    out = np.empty((B, H), dtype=np.float32)
+    _load().oracle_token_tree_f32(_p(a), _p(out), B, S, H)
+    return out
+
+
+def bwd_products_f32(dy, x, mean, rstd):
+    dy, x = _c(dy, np.uint16), _c(x, np.uint16)
+    mean, rstd = _c(mean, np.float32), _c(rstd, np.float32)
+    B, S, D = x.shape
+    prod = np.empty((B, S, 2 * D), dtype=np.float32)
+    _load().oracle_bwd_products_f32(_p(dy), _p(x), _p(mean), _p(rstd), _p(prod), B, S, D)
+    return prod
+
+
+# --- projection backward --------------------------------------------------
+
+def proj_bwd(d_emb, temb, W, want_dW=True):
+    """(d_temb bf16 bits [B,D], dW fp64 [2D,D] or None, db fp64 [2D])."""
+    d_emb, temb, W = _c(d_emb, np.float32), _c(temb, np.uint16), _c(W, np.uint16)
+    B, D = temb.shape
+    d_temb = np.empty((B, D), dtype=np.uint16)
+    dW = np.empty((2 * D, D), dtype=np.float64) if want_dW else None
+    db = np.empty(2 * D, dtype=np.float64)
+    _load().oracle_proj_bwd(_p(d_emb), _p(temb), _p(W), _p(d_temb), _p(dW), _p(db), B, D)
+    return d_temb, dW, db
+
+
+def proj_bwd_f64(d_emb, temb, W):
+    d_emb, temb, W = _c(d_emb, np.float64), _c(temb, np.float64), _c(W, np.float64)
+    B, D = temb.shape
+    d_temb = np.empty((B, D), dtype=np.float64)
+    dW = np.empty((2 * D, D), dtype=np.float64)
+    db = np.empty(2 * D, dtype=np.float64)
+    _load().oracle_proj_bwd_f64(_p(d_emb), _p(temb), _p(W), _p(d_temb), _p(dW), _p(db), B, D)
+    return d_temb, dW, db
+
+
+def wgrad_seq_f32(d_emb, temb, dW_acc=None, db_acc=None, accumulate=False):
+    """(dW_acc fp32 [2D,D], db_acc fp32 [2D]) in the operator's sequential order."""
+    d_emb, temb = _c(d_emb, np.float32), _c(temb, np.uint16)
+    B, D = temb.shape
+    dW = np.zeros((2 * D, D), np.float32) if dW_acc is None else np.array(dW_acc, dtype=np.float32, copy=True)
+    db = np.zeros(2 * D, np.float32) if db_acc is None else np.array(db_acc, dtype=np.float32, copy=True)
+    _load().oracle_wgrad_seq_f32(_p(d_emb), _p(temb), _p(dW), _p(db), int(bool(accumulate)), B, D)
+    return dW, db
+
+
+def bf16_from_f64(a):
+    a = _c(a, np.float64)
+    h = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_bf16_from_f64(_p(a), _p(h), a.size)
+    return h

@@ -1,0 +1,537 @@
+/*
+ * CPU oracle for the batch-invariant DiT AdaLN final modulation ("norm_out"),
+ * forward and backward.
+ *
+ * TEST INFRASTRUCTURE.  This is a plain, slow, obviously-correct host
+ * implementation used only to check the CUDA library: the tests, the smoke
+ * check and the benchmark's CPU-baseline leg load it, nothing else does.  It
+ * shares no code, header, table or helper with the CUDA path.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared -lm
+ * (no contraction into FMA, IEEE single/double arithmetic as written).
+ *
+ * What it computes (sources):
+ *
+ *  [op]    RL-Kernel PR 538 "final_adaln_out", section "What":
+ *            scale, shift = (SiLU(temb) @ W^T + b).chunk(2)   (3072 -> 6144,
+ *                                                              scale first)
+ *            out = LayerNorm(x, eps=1e-6, no affine) * (1 + scale) + shift
+ *          and the backward: dx, d_scale/d_shift as token sums, dW/db/d_temb.
+ *  [round] miles_diffusion PR 108 "bitwise train<->rollout parity via
+ *          autocast-parity norms and a pinned flash kernel", Summary, root
+ *          cause 1 (and its second rendering, "Patches"): LayerNorm computes
+ *          and returns fp32, (1 + scale) rounds once in bf16, the modulation
+ *          promotes to fp32, one bf16 rounding at the store.
+ *  [tree]  RL-Kernel PR 538, section "What" (token sums by a fixed 32-way
+ *          balanced tree whose shape depends only on the sequence length) and
+ *          the review thread on the cancellation case (each 32-token tile is
+ *          summed in ascending order with Neumaier compensation; tile sums and
+ *          corrections are folded level by level; one final IEEE add).
+ *  [ref]   RL-Kernel PR 538, section "What": an independent CPU reference with
+ *          sequential Neumaier token sums; review findings ask for a
+ *          compensated input gradient and bias gradient as well.
+ *
+ * Every sum here is a sequential Neumaier sum in fp64 (compensated, so it is
+ * correct to about one fp64 ulp), every product of two bf16 values or of a
+ * bf16 and an fp32 value is exact in fp64, and the only roundings are the
+ * ones the operator defines.  Readings of points the pages leave open:
+ *
+ *  - LayerNorm variance is the biased one (divide by D), eps = fp32(1e-6) is
+ *    added to the variance inside the square root.
+ *  - SiLU output u is bf16(silu(t)), the nearest bf16 to the exact value.
+ *  - The projection bias is added before the single bf16 rounding of emb.
+ *  - onep = bf16(fp32(1 + scale)); m = fp32(fp32(xhat * onep) + shift), xhat
+ *    being the fp32 rounding of the exact LayerNorm value; out = bf16(m).
+ *  - d_scale[b,d] = sum_s g*xhat (xhat the fp32 forward value), d_shift[b,d]
+ *    = sum_s g, g = fp32(dy); both returned in fp32.
+ *  - dx = bf16(exact LayerNorm backward of g*onep).
+ *  - The projection backward takes e = bf16(d_emb); d_temb = bf16(d_silu *
+ *    silu'(t)); dW = sum_b e*u, db = sum_b e.
+ *
+ * The fp32 token tree (oracle_token_tree_f32) and the fp32 sequential weight
+ * gradient (oracle_wgrad_seq_f32) replay the operator's own fixed orders in
+ * fp32 from their definitions above, so that the library's results can be
+ * checked bit for bit.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+static float f32_from_bits(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t bits_from_f32(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+static float bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
+static double bf16_to_f64(uint16_t h) { return (double)bf16_to_f32(h); }
+
+/* nearest bf16 to a float (ties to even) */
+static uint16_t bf16_from_f32(float f)
+{
+    uint32_t u = bits_from_f32(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* nearest bf16 to a double (ties to even), rounded once, not through fp32 */
+static uint16_t bf16_from_f64(double x)
+{
+    if (x != x) return 0x7FC0u;
+    if (x == 0.0) return signbit(x) ? 0x8000u : 0x0000u;
+    double a = fabs(x);
+    int e;
+    frexp(a, &e);            /* a = m * 2^e, 0.5 <= m < 1 */
+    int q = e - 8;           /* spacing of 8 significant bits */
+    if (q < -133) q = -133;  /* bf16 subnormal spacing 2^-133 */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    float rf = (float)r;     /* exact (or overflow to inf) */
+    uint16_t h = (uint16_t)(bits_from_f32(rf) >> 16);
+    return x < 0 ? (uint16_t)(h | 0x8000u) : h;
+}
+
+/* ------------------------------------------------------------------------ */
+/* compensated summation in fp64                                             */
+/* ------------------------------------------------------------------------ */
+
+typedef struct { double s, c; } nsum;
+
+static void nsum_add(nsum *a, double v)
+{
+    double t = a->s + v;
+    if (fabs(a->s) >= fabs(v)) a->c += (a->s - t) + v;
+    else                       a->c += (v - t) + a->s;
+    a->s = t;
+}
+static double nsum_val(const nsum *a) { return a->s + a->c; }
+
+/* ------------------------------------------------------------------------ */
+/* SiLU and its derivative, fp64                                             */
+/* ------------------------------------------------------------------------ */
+
+static double sigmoid64(double t) { return 1.0 / (1.0 + exp(-t)); }
+static double silu64(double t) { return t * sigmoid64(t); }
+/* d/dt [t * sigma(t)] = sigma(t) * (1 + t * (1 - sigma(t)))               */
+static double dsilu64(double t) { double s = sigmoid64(t); return s * (1.0 + t * (1.0 - s)); }
+
+void oracle_silu_bf16(const uint16_t *t, uint16_t *u, long n)
+{
+    for (long i = 0; i < n; ++i) u[i] = bf16_from_f64(silu64(bf16_to_f64(t[i])));
+}
+
+void oracle_dsilu_f64(const double *t, double *out, long n)
+{
+    for (long i = 0; i < n; ++i) out[i] = dsilu64(t[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* shared cores                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* emb[b,n] = sum_k u[b,k] * W[n,k] + bias[n], compensated fp64 */
+static void proj_core(const double *u, const double *W, const double *bias,
+                      double *emb, int B, int K, int N)
+{
+    for (int b = 0; b < B; ++b)
+        for (int n = 0; n < N; ++n) {
+            nsum acc = {0.0, 0.0};
+            const double *w = W + (size_t)n * K;
+            const double *ub = u + (size_t)b * K;
+            for (int k = 0; k < K; ++k) nsum_add(&acc, ub[k] * w[k]);
+            nsum_add(&acc, bias[n]);
+            emb[(size_t)b * N + n] = nsum_val(&acc);
+        }
+}
+
+/* LayerNorm of one row (no affine): biased variance, eps inside the sqrt */
+static void ln_row(const double *x, int D, double eps, double *mu_out,
+                   double *rstd_out, double *xhat)
+{
+    nsum s = {0.0, 0.0};
+    for (int d = 0; d < D; ++d) nsum_add(&s, x[d]);
+    double mu = nsum_val(&s) / D;
+    nsum v = {0.0, 0.0};
+    for (int d = 0; d < D; ++d) { double c = x[d] - mu; nsum_add(&v, c * c); }
+    double var = nsum_val(&v) / D;
+    double rstd = 1.0 / sqrt(var + eps);
+    for (int d = 0; d < D; ++d) xhat[d] = (x[d] - mu) * rstd;
+    *mu_out = mu;
+    *rstd_out = rstd;
+}
+
+/* LayerNorm backward of one row: given the upstream gradient gh of the
+ * normalised value, dx = rstd * (gh - mean(gh) - xhat * mean(gh * xhat)).   */
+static void ln_bwd_row(const double *gh, const double *xhat, double rstd, int D,
+                       double *dx)
+{
+    nsum s1 = {0.0, 0.0}, s2 = {0.0, 0.0};
+    for (int d = 0; d < D; ++d) { nsum_add(&s1, gh[d]); nsum_add(&s2, gh[d] * xhat[d]); }
+    double c1 = nsum_val(&s1) / D;
+    double c2 = nsum_val(&s2) / D;
+    for (int d = 0; d < D; ++d) dx[d] = rstd * (gh[d] - c1 - xhat[d] * c2);
+}
+
+/* ------------------------------------------------------------------------ */
+/* projection forward                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* emb = bf16( bf16(silu(temb)) @ W^T + b ); W is [2D, D] row-major,
+ * emb [B, 2D] = [scale | shift].                                            */
+void oracle_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
+                     uint16_t *emb, int B, int D)
+{
+    int N = 2 * D;
+    double *u = malloc(sizeof(double) * (size_t)B * D);
+    double *w = malloc(sizeof(double) * (size_t)N * D);
+    double *bb = malloc(sizeof(double) * (size_t)N);
+    double *e = malloc(sizeof(double) * (size_t)B * N);
+    for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f64(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
+    for (size_t i = 0; i < (size_t)N * D; ++i) w[i] = bf16_to_f64(W[i]);
+    for (int n = 0; n < N; ++n) bb[n] = bf16_to_f64(bias[n]);
+    proj_core(u, w, bb, e, B, D, N);
+    for (size_t i = 0; i < (size_t)B * N; ++i) emb[i] = bf16_from_f64(e[i]);
+    free(u); free(w); free(bb); free(e);
+}
+
+/* the same map without any rounding */
+void oracle_proj_fwd_f64(const double *temb, const double *W, const double *bias,
+                         double *emb, int B, int D)
+{
+    int N = 2 * D;
+    double *u = malloc(sizeof(double) * (size_t)B * D);
+    for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = silu64(temb[i]);
+    proj_core(u, W, bias, emb, B, D, N);
+    free(u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm + modulation forward                                            */
+/* ------------------------------------------------------------------------ */
+
+/* out = bf16( fp32( fp32(xhat * onep) + shift ) ), onep = bf16(fp32(1+scale)),
+ * xhat = fp32(exact LayerNorm).  mean/rstd: fp32 roundings of the exact row
+ * statistics (nullable).                                                     */
+void oracle_out_fwd(const uint16_t *x, const uint16_t *emb, float eps, uint16_t *out,
+                    float *mean, float *rstd, int B, int S, int D)
+{
+    double *xr = malloc(sizeof(double) * (size_t)D);
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    float *onep = malloc(sizeof(float) * (size_t)D);
+    float *shift = malloc(sizeof(float) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        const uint16_t *e = emb + (size_t)b * 2 * D;
+        for (int d = 0; d < D; ++d) {
+            onep[d] = bf16_to_f32(bf16_from_f32(1.0f + bf16_to_f32(e[d])));
+            shift[d] = bf16_to_f32(e[D + d]);
+        }
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            const uint16_t *xs = x + row * D;
+            for (int d = 0; d < D; ++d) xr[d] = bf16_to_f64(xs[d]);
+            double mu, r;
+            ln_row(xr, D, (double)eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d) {
+                float xf = (float)xh[d];
+                float prod = xf * onep[d];
+                float m = prod + shift[d];
+                out[row * D + d] = bf16_from_f32(m);
+            }
+            if (mean) mean[row] = (float)mu;
+            if (rstd) rstd[row] = (float)r;
+        }
+    }
+    free(xr); free(xh); free(onep); free(shift);
+}
+
+/* out = LayerNorm(x) * (1 + scale) + shift, everything fp64, no rounding */
+void oracle_out_fwd_f64(const double *x, const double *scale, const double *shift,
+                        double eps, double *out, int B, int S, int D)
+{
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            double mu, r;
+            ln_row(x + row * D, D, eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d)
+                out[row * D + d] = xh[d] * (1.0 + scale[(size_t)b * D + d]) + shift[(size_t)b * D + d];
+        }
+    free(xh);
+}
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm + modulation backward                                           */
+/* ------------------------------------------------------------------------ */
+
+/* dx = bf16(LayerNorm backward of g*onep), g = fp32(dy);
+ * d_emb[b, 0:D]  = d_scale = sum_s g * xhat_f32,
+ * d_emb[b, D:2D] = d_shift = sum_s g,
+ * token sums sequential over s (ascending) with Neumaier compensation in
+ * fp64, returned rounded to fp32.  xhat is recomputed from x.               */
+void oracle_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, float eps,
+                    uint16_t *dx, float *d_emb, int B, int S, int D)
+{
+    double *xr = malloc(sizeof(double) * (size_t)D);
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    double *gh = malloc(sizeof(double) * (size_t)D);
+    double *dxr = malloc(sizeof(double) * (size_t)D);
+    double *onep = malloc(sizeof(double) * (size_t)D);
+    nsum *ss = malloc(sizeof(nsum) * (size_t)D);
+    nsum *sh = malloc(sizeof(nsum) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        const uint16_t *e = emb + (size_t)b * 2 * D;
+        for (int d = 0; d < D; ++d) {
+            onep[d] = (double)bf16_to_f32(bf16_from_f32(1.0f + bf16_to_f32(e[d])));
+            ss[d].s = ss[d].c = 0.0;
+            sh[d].s = sh[d].c = 0.0;
+        }
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            for (int d = 0; d < D; ++d) xr[d] = bf16_to_f64(x[row * D + d]);
+            double mu, r;
+            ln_row(xr, D, (double)eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d) {
+                double g = bf16_to_f64(dy[row * D + d]);
+                gh[d] = g * onep[d];                   /* exact */
+                nsum_add(&ss[d], g * (double)(float)xh[d]); /* exact product */
+                nsum_add(&sh[d], g);
+            }
+            ln_bwd_row(gh, xh, r, D, dxr);
+            for (int d = 0; d < D; ++d) dx[row * D + d] = bf16_from_f64(dxr[d]);
+        }
+        for (int d = 0; d < D; ++d) {
+            d_emb[(size_t)b * 2 * D + d] = (float)nsum_val(&ss[d]);
+            d_emb[(size_t)b * 2 * D + D + d] = (float)nsum_val(&sh[d]);
+        }
+    }
+    free(xr); free(xh); free(gh); free(dxr); free(onep); free(ss); free(sh);
+}
+
+/* exact gradients of oracle_out_fwd_f64 for upstream gradient dy */
+void oracle_out_bwd_f64(const double *dy, const double *x, const double *scale, double eps,
+                        double *dx, double *d_scale, double *d_shift, int B, int S, int D)
+{
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    double *gh = malloc(sizeof(double) * (size_t)D);
+    nsum *ss = malloc(sizeof(nsum) * (size_t)D);
+    nsum *sh = malloc(sizeof(nsum) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) { ss[d].s = ss[d].c = 0.0; sh[d].s = sh[d].c = 0.0; }
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            double mu, r;
+            ln_row(x + row * D, D, eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d) {
+                double g = dy[row * D + d];
+                gh[d] = g * (1.0 + scale[(size_t)b * D + d]);
+                nsum_add(&ss[d], g * xh[d]);
+                nsum_add(&sh[d], g);
+            }
+            ln_bwd_row(gh, xh, r, D, dx + row * D);
+        }
+        for (int d = 0; d < D; ++d) {
+            d_scale[(size_t)b * D + d] = nsum_val(&ss[d]);
+            d_shift[(size_t)b * D + d] = nsum_val(&sh[d]);
+        }
+    }
+    free(xh); free(gh); free(ss); free(sh);
+}
+
+/* ------------------------------------------------------------------------ */
+/* token sums                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* out[b,h] = sum_s in[b,s,h], sequential in s with Neumaier compensation (fp64) */
+void oracle_token_sum_f64(const float *in, double *out, int B, int S, int H)
+{
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            nsum a = {0.0, 0.0};
+            for (int s = 0; s < S; ++s) nsum_add(&a, (double)in[((size_t)b * S + s) * H + h]);
+            out[(size_t)b * H + h] = nsum_val(&a);
+        }
+}
+
+/* one Neumaier step in fp32: t = s + v; the part of the smaller operand lost
+ * in t goes into the compensation c.  |s| == |v| takes the first branch.     */
+static void nstep_f32(float *s, float *c, float v)
+{
+    float t = *s + v;
+    float lost;
+    if (fabsf(*s) >= fabsf(v)) { float d = *s - t; lost = d + v; }
+    else                       { float d = v - t;  lost = d + *s; }
+    *c = *c + lost;
+    *s = t;
+}
+
+#define TREE_FAN 32
+
+/* The fixed 32-way token tree, in fp32:
+ *  level 0: tokens are cut into tiles of 32 (the last tile may be short);
+ *           each tile is a Neumaier sum over its tokens in ascending order,
+ *           starting from its first token: node = (sum, correction);
+ *  level l>=1: nodes of level l-1 are cut into groups of 32 (the last group
+ *           may be short); a group's sum is the Neumaier sum of its
+ *           children's sums in ascending order (starting from the first
+ *           child), with compensation c; its correction is
+ *           c + (((k0 + k1) + k2) + ...), the children's corrections added in
+ *           ascending order;
+ *  the root is the first level with one node; the result is sum + correction.
+ * The shape depends only on S.                                              */
+static float tree32_column(const float *v, long stride, int S)
+{
+    int n = (S + TREE_FAN - 1) / TREE_FAN;
+    float *sig = malloc(sizeof(float) * (size_t)n);
+    float *kap = malloc(sizeof(float) * (size_t)n);
+    for (int t = 0; t < n; ++t) {
+        int r0 = t * TREE_FAN, r1 = r0 + TREE_FAN < S ? r0 + TREE_FAN : S;
+        float s = v[(long)r0 * stride], c = 0.0f;
+        for (int r = r0 + 1; r < r1; ++r) nstep_f32(&s, &c, v[(long)r * stride]);
+        sig[t] = s;
+        kap[t] = c;
+    }
+    while (n > 1) {
+        int m = (n + TREE_FAN - 1) / TREE_FAN;
+        for (int g = 0; g < m; ++g) {
+            int i0 = g * TREE_FAN, i1 = i0 + TREE_FAN < n ? i0 + TREE_FAN : n;
+            float s = sig[i0], c = 0.0f, k = kap[i0];
+            for (int i = i0 + 1; i < i1; ++i) { nstep_f32(&s, &c, sig[i]); k = k + kap[i]; }
+            sig[g] = s;          /* g <= i0: children already consumed */
+            kap[g] = c + k;
+        }
+        n = m;
+    }
+    float res = sig[0] + kap[0];
+    free(sig);
+    free(kap);
+    return res;
+}
+
+/* out[b,h] = the fixed 32-way tree sum over s of in[b,s,h] (S >= 1) */
+void oracle_token_tree_f32(const float *in, float *out, int B, int S, int H)
+{
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            out[(size_t)b * H + h] = tree32_column(in + (size_t)b * S * H + h, H, S);
+}
+
+/* The backward's token products as the operator defines them in fp32, from
+ * the forward's saved row statistics: xhat = fp32(fp32(x - mean) * rstd),
+ * g = fp32(dy); prod[b,s,0:D] = fp32(g * xhat), prod[b,s,D:2D] = g.          */
+void oracle_bwd_products_f32(const uint16_t *dy, const uint16_t *x, const float *mean,
+                             const float *rstd, float *prod, int B, int S, int D)
+{
+    for (size_t row = 0; row < (size_t)B * S; ++row)
+        for (int d = 0; d < D; ++d) {
+            float xc = bf16_to_f32(x[row * D + d]) - mean[row];
+            float xh = xc * rstd[row];
+            float g = bf16_to_f32(dy[row * D + d]);
+            prod[row * 2 * D + d] = g * xh;
+            prod[row * 2 * D + D + d] = g;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* projection backward                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* e = bf16(d_emb); u = bf16(silu(temb));
+ * d_temb[b,k] = bf16( (sum_n e[b,n] W[n,k]) * silu'(temb[b,k]) );
+ * dW[n,k] = sum_b e[b,n] u[b,k];  db[n] = sum_b e[b,n]   (fp64, compensated) */
+void oracle_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *W,
+                     uint16_t *d_temb, double *dW, double *db, int B, int D)
+{
+    int N = 2 * D;
+    double *e = malloc(sizeof(double) * (size_t)B * N);
+    double *u = malloc(sizeof(double) * (size_t)B * D);
+    nsum *acc = malloc(sizeof(nsum) * (size_t)D);
+    for (size_t i = 0; i < (size_t)B * N; ++i) e[i] = bf16_to_f64(bf16_from_f32(d_emb[i]));
+    for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f64(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
+    for (int b = 0; b < B; ++b) {
+        for (int k = 0; k < D; ++k) acc[k].s = acc[k].c = 0.0;
+        for (int n = 0; n < N; ++n) {
+            double en = e[(size_t)b * N + n];
+            const uint16_t *w = W + (size_t)n * D;
+            for (int k = 0; k < D; ++k) nsum_add(&acc[k], en * bf16_to_f64(w[k]));
+        }
+        for (int k = 0; k < D; ++k) {
+            double t = bf16_to_f64(temb[(size_t)b * D + k]);
+            d_temb[(size_t)b * D + k] = bf16_from_f64(nsum_val(&acc[k]) * dsilu64(t));
+        }
+    }
+    if (dW || db)
+        for (int n = 0; n < N; ++n) {
+            if (dW)
+                for (int k = 0; k < D; ++k) {
+                    nsum a = {0.0, 0.0};
+                    for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n] * u[(size_t)b * D + k]);
+                    dW[(size_t)n * D + k] = nsum_val(&a);
+                }
+            if (db) {
+                nsum a = {0.0, 0.0};
+                for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n]);
+                db[n] = nsum_val(&a);
+            }
+        }
+    free(e); free(u); free(acc);
+}
+
+/* exact gradients of oracle_proj_fwd_f64 for upstream gradient d_emb */
+void oracle_proj_bwd_f64(const double *d_emb, const double *temb, const double *W,
+                         double *d_temb, double *dW, double *db, int B, int D)
+{
+    int N = 2 * D;
+    for (int b = 0; b < B; ++b)
+        for (int k = 0; k < D; ++k) {
+            nsum a = {0.0, 0.0};
+            for (int n = 0; n < N; ++n) nsum_add(&a, d_emb[(size_t)b * N + n] * W[(size_t)n * D + k]);
+            d_temb[(size_t)b * D + k] = nsum_val(&a) * dsilu64(temb[(size_t)b * D + k]);
+        }
+    for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < D; ++k) {
+            nsum a = {0.0, 0.0};
+            for (int b = 0; b < B; ++b) nsum_add(&a, d_emb[(size_t)b * N + n] * silu64(temb[(size_t)b * D + k]));
+            dW[(size_t)n * D + k] = nsum_val(&a);
+        }
+        nsum a = {0.0, 0.0};
+        for (int b = 0; b < B; ++b) nsum_add(&a, d_emb[(size_t)b * N + n]);
+        db[n] = nsum_val(&a);
+    }
+}
+
+/* The weight gradient in the operator's fixed order, fp32: starting from the
+ * caller's accumulators (accumulate != 0) or from +0, samples are added in
+ * ascending order, acc = acc + e[b,n] * u[b,k] (the product of two bf16
+ * values is exact in fp32), db_acc[n] = db_acc[n] + e[b,n].                 */
+void oracle_wgrad_seq_f32(const float *d_emb, const uint16_t *temb, float *dW_acc,
+                          float *db_acc, int accumulate, int B, int D)
+{
+    int N = 2 * D;
+    float *e = malloc(sizeof(float) * (size_t)B * N);
+    float *u = malloc(sizeof(float) * (size_t)B * D);
+    for (size_t i = 0; i < (size_t)B * N; ++i) e[i] = bf16_to_f32(bf16_from_f32(d_emb[i]));
+    for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f32(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
+    for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < D; ++k) {
+            float a = accumulate ? dW_acc[(size_t)n * D + k] : 0.0f;
+            for (int b = 0; b < B; ++b) a = a + e[(size_t)b * N + n] * u[(size_t)b * D + k];
+            dW_acc[(size_t)n * D + k] = a;
+        }
+        float a = accumulate ? db_acc[n] : 0.0f;
+        for (int b = 0; b < B; ++b) a = a + e[(size_t)b * N + n];
+        db_acc[n] = a;
+    }
+    free(e); free(u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* format helpers exported for the tests                                     */
+/* ------------------------------------------------------------------------ */
+
+void oracle_bf16_from_f64(const double *x, uint16_t *h, long n)
+{
+    for (long i = 0; i < n; ++i) h[i] = bf16_from_f64(x[i]);
+}

@@ -1,0 +1,539 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test ties one oracle function to one of: a value the pages print (the
+token-tree cancellation result, the SiLU derivative at 1), exact rational
+arithmetic on small inputs, an independent library routine (PyTorch's fp64
+LayerNorm, linear, SiLU and autograd on the CPU; math.fsum), a closed form or
+an invariant of the mathematics, or finite differences.  They are chosen so
+that a dropped term, a wrong sign or index, a transposed operand, a missing
+rounding point or a swapped (scale, shift) order fails at least one of them.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_dit_adaln_gb300 import synth
+from tolerance import assert_bitwise, bf16_to_f64, bf16_ulp_dist
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+EPS32 = float(np.float32(1e-6))
+
+
+def golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# exact bf16 rounding, written with rationals (independent of the oracle's)
+# ---------------------------------------------------------------------------
+
+def bf16_exact_round(v: Fraction) -> int:
+    """Bits of the bf16 nearest to the rational v (ties to even)."""
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    # a in [2^e, 2^(e+1)); spacing 2^(e-7) for normals, 2^-133 below 2^-126
+    q = max(e - 7, -133)
+    scaled = a / (Fraction(2) ** q)
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = Fraction(n) * Fraction(2) ** q
+    f = np.float32(float(val))
+    assert Fraction(float(f)) == val
+    return sign | int(np.array([f], dtype=np.float32).view(np.uint32)[0] >> 16)
+
+
+def test_bf16_rounding_from_f64_matches_exact(orc):
+    rng = np.random.default_rng(1)
+    vals = list(rng.standard_normal(3000) * np.exp2(rng.integers(-140, 120, 3000)))
+    # ties and near-ties, subnormals, zeros
+    for k in range(0, 256, 7):
+        base = 1.0 + k / 128.0
+        vals += [base + 1 / 256.0, -(base + 1 / 256.0), np.nextafter(base + 1 / 256.0, 10), np.nextafter(base + 1 / 256.0, 0)]
+    vals += [2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -135, 2.0 ** -126 * 1.5, 0.0, -0.0, 2.0 ** 127 * 1.9921875]
+    x = np.array(vals, dtype=np.float64)
+    got = orc.bf16_from_f64(x)
+    want = np.array([bf16_exact_round(Fraction(float(v))) if v != 0 else (0x8000 if math.copysign(1, v) < 0 else 0)
+                     for v in x], dtype=np.uint16)
+    assert_bitwise(got, want, "bf16 from fp64")
+
+
+# ---------------------------------------------------------------------------
+# SiLU and its derivative
+# ---------------------------------------------------------------------------
+
+def test_silu_derivative_worked_value(orc):
+    (t, want, tol), = golden_rows("silu_vjp.txt")
+    got = orc.dsilu_f64(np.array([float(t)]))[0]
+    assert abs(got - float(want)) <= float(tol)
+    # and the derivative is the derivative: central differences of t*sigmoid(t)
+    ts = np.linspace(-8, 8, 33)
+    h = 1e-6
+    fd = ((ts + h) / (1 + np.exp(-(ts + h))) - (ts - h) / (1 + np.exp(-(ts - h)))) / (2 * h)
+    np.testing.assert_allclose(orc.dsilu_f64(ts), fd, rtol=1e-8, atol=1e-9)
+
+
+def test_silu_bf16_is_nearest_bf16_of_exact_silu(orc):
+    import mpmath
+    mpmath.mp.prec = 200
+    # every bf16 with |t| in a useful range, sampled; plus the extremes
+    all_bits = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    fin = all_bits[(all_bits & 0x7F80) != 0x7F80]
+    rng = np.random.default_rng(2)
+    pick = np.concatenate([rng.choice(fin, 3000, replace=False),
+                           np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x0001, 0x8001, 0x7F7F, 0xFF7F], np.uint16)])
+    got = orc.silu_bf16(pick)
+    want = []
+    for h in pick:
+        t = mpmath.mpf(float(bf16_to_f64(np.array([h]))[0]))
+        s = t / (1 + mpmath.exp(-t))
+        if abs(s) < mpmath.mpf(2) ** -135:  # below half the smallest bf16 subnormal
+            want.append(0x8000 if t < 0 else 0)
+        else:
+            mag = Fraction(int(s.man)) * Fraction(2) ** int(s.exp)  # mpmath keeps the sign apart
+            want.append(bf16_exact_round(-mag if s < 0 else mag))
+    want = np.array(want, dtype=np.uint16)
+    # The oracle rounds the fp64 value of t / (1 + exp(-t)).  For |t| < 2^-125
+    # that value is t/2 exactly (the t^2/4 term is below fp64 resolution) and
+    # falls in the bf16 subnormal range, where an odd t makes it a bf16 tie; the
+    # exact value lies just off the tie.  Those inputs are the only ones allowed
+    # to differ, by one ulp.
+    subnormal = (pick & 0x7F80) <= 0x0080
+    dist = bf16_ulp_dist(got, want)  # +0 and -0 count as equal
+    mism = np.flatnonzero(dist != 0)
+    assert np.all(subnormal[mism]), [(hex(pick[i]), hex(got[i]), hex(want[i])) for i in mism[:5]]
+    assert np.all(dist[mism] == 1)
+    t = bf16_to_f64(pick[subnormal])
+    assert_bitwise(got[subnormal], orc.bf16_from_f64(t / 2.0), "tiny t: u = bf16(t/2)")
+
+
+# ---------------------------------------------------------------------------
+# projection forward
+# ---------------------------------------------------------------------------
+
+def _bf16(a):
+    return synth.bf16_bits_from_f32(np.asarray(a, dtype=np.float32))
+
+
+def test_proj_fwd_exact_rational_small(orc):
+    """emb must be the nearest bf16 of the exact sum u.W + b, u = bf16(silu(t))."""
+    rng = np.random.default_rng(3)
+    B, D = 2, 16
+    temb = _bf16(rng.standard_normal((B, D)))
+    W = _bf16(rng.standard_normal((2 * D, D)) * 0.3)
+    b = _bf16(rng.standard_normal(2 * D) * 0.3)
+    u = orc.silu_bf16(temb)  # pinned above
+    uf = bf16_to_f64(u)
+    Wf = bf16_to_f64(W)
+    bf = bf16_to_f64(b)
+    got = orc.proj_fwd(temb, W, b)
+    for i in range(B):
+        for n in range(2 * D):
+            exact = sum(Fraction(float(uf[i, k])) * Fraction(float(Wf[n, k])) for k in range(D)) + Fraction(float(bf[n]))
+            assert got[i, n] == bf16_exact_round(exact) if exact != 0 else True, (i, n)
+
+
+def test_proj_fwd_special_cases_and_order(orc):
+    rng = np.random.default_rng(4)
+    B, D = 3, 32
+    temb = _bf16(rng.standard_normal((B, D)))
+    W = _bf16(rng.standard_normal((2 * D, D)) * 0.02)
+    b = _bf16(rng.standard_normal(2 * D) * 0.02)
+    # W = 0 -> emb = b bitwise
+    assert_bitwise(orc.proj_fwd(temb, np.zeros_like(W), b), np.broadcast_to(b, (B, 2 * D)), "W=0")
+    # temb = 0 -> silu = 0 -> emb = b
+    assert_bitwise(orc.proj_fwd(np.zeros_like(temb), W, b), np.broadcast_to(b, (B, 2 * D)), "temb=0")
+    # (scale, shift) order: zeroing the second half of W leaves emb[:, D:] = b[D:]
+    W2 = W.copy()
+    W2[D:] = 0
+    e2 = orc.proj_fwd(temb, W2, b)
+    assert_bitwise(e2[:, D:], np.broadcast_to(b[D:], (B, D)), "shift half")
+    assert_bitwise(e2[:, :D], orc.proj_fwd(temb, W, b)[:, :D], "scale half")
+
+
+def test_proj_fwd_f64_matches_torch(orc):
+    rng = np.random.default_rng(5)
+    B, D = 3, 24
+    temb = rng.standard_normal((B, D))
+    W = rng.standard_normal((2 * D, D)) * 0.1
+    b = rng.standard_normal(2 * D) * 0.1
+    ref = torch.nn.functional.linear(torch.nn.functional.silu(torch.from_numpy(temb)),
+                                     torch.from_numpy(W), torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(orc.proj_fwd_f64(temb, W, b), ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm + modulation forward
+# ---------------------------------------------------------------------------
+
+def test_out_fwd_f64_matches_torch(orc):
+    rng = np.random.default_rng(6)
+    B, S, D = 2, 5, 40
+    x = rng.standard_normal((B, S, D)) * 3 + 0.5
+    x[1, 2] *= 50
+    scale = rng.standard_normal((B, D)) * 0.1
+    shift = rng.standard_normal((B, D)) * 0.1
+    tx = torch.from_numpy(x)
+    ref = (torch.nn.functional.layer_norm(tx, (D,), eps=1e-6) * (1 + torch.from_numpy(scale)[:, None, :])
+           + torch.from_numpy(shift)[:, None, :]).numpy()
+    np.testing.assert_allclose(orc.out_fwd_f64(x, scale, shift, 1e-6), ref, rtol=1e-11, atol=1e-12)
+
+
+def test_out_fwd_reduces_to_plain_layernorm_when_W_and_b_are_zero(orc):
+    """W = b = 0 -> emb = 0 -> onep = 1, shift = 0 -> out = bf16(fp32(LN(x)))."""
+    rng = np.random.default_rng(7)
+    B, S, D = 2, 7, 64
+    x = _bf16(rng.standard_normal((B, S, D)) * 2)
+    emb = orc.proj_fwd(_bf16(rng.standard_normal((B, D))), np.zeros((2 * D, D), np.uint16), np.zeros(2 * D, np.uint16))
+    assert not emb.any()
+    out, mean, rstd = orc.out_fwd(x, emb)
+    xf = torch.from_numpy(bf16_to_f64(x))
+    ln = torch.nn.functional.layer_norm(xf, (D,), eps=EPS32).numpy()
+    want = synth.bf16_bits_from_f32(ln.astype(np.float32))
+    assert_bitwise(out, want, "plain LN")
+    np.testing.assert_array_equal(mean, xf.mean(-1).numpy().astype(np.float32))
+    var = xf.var(-1, unbiased=False).numpy()
+    np.testing.assert_array_equal(rstd, (1.0 / np.sqrt(var + EPS32)).astype(np.float32))
+
+
+def test_out_fwd_invariants(orc):
+    rng = np.random.default_rng(8)
+    B, S, D = 1, 4, 256
+    x = rng.standard_normal((B, S, D)) * 4 - 1
+    xh = orc.out_fwd_f64(x, np.zeros((B, D)), np.zeros((B, D)), 1e-6)
+    var = x.var(-1)
+    np.testing.assert_allclose(xh.mean(-1), 0, atol=1e-13)
+    np.testing.assert_allclose(xh.var(-1), var / (var + 1e-6), rtol=1e-12)
+    # constant row -> xhat = 0 exactly -> out = shift bitwise
+    xc = np.full((1, 3, D), 0x3FC0, np.uint16)  # 1.5
+    emb = _bf16(rng.standard_normal((1, 2 * D)))
+    out, mean, rstd = orc.out_fwd(xc, emb)
+    assert_bitwise(out, np.broadcast_to(emb[:, D:], (1, 3, D)).astype(np.uint16), "constant row")
+    assert np.all(mean == 1.5)
+
+
+def _pm_one_row(D):
+    return np.tile(np.array([0xBF80, 0x3F80], np.uint16), D // 2)  # -1, +1, ...: mean 0, var 1
+
+
+def test_out_fwd_rounding_point_onep(orc):
+    """Worked example of '(1 + scale) rounds once in bf16'.
+
+    x = (-1, +1, ...): mean 0, variance 1, xhat = +-1/sqrt(1 + eps) = +-0.99999952
+    (fp32).  bf16 values in [1, 2) are 2^-7 apart.  scale = 3 * 2^-8: 1 + scale =
+    1.01171875 is the midpoint of 1 + 2^-7 and 1 + 2^-6; ties-to-even gives
+    onep = 1 + 2^-6.  With shift = 0, m = 0.99999952 * 1.015625 = 1.0156245,
+    so out = 1 + 2^-6 on the +1 entries.  Without the rounding of (1 + scale),
+    m = 0.99999952 * 1.01171875 = 1.0117183 lies below the midpoint and out
+    would be 1 + 2^-7."""
+    D = 8
+    x = _pm_one_row(D).reshape(1, 1, D)
+    emb = np.zeros((1, 2 * D), np.uint16)
+    emb[0, :D] = _bf16(np.full(D, 3 * 2.0 ** -8))
+    assert np.all(bf16_to_f64(emb[0, :D]) == 3 * 2.0 ** -8)
+    out, _, _ = orc.out_fwd(x, emb)
+    vals = bf16_to_f64(out[0, 0])
+    assert np.all(vals[1::2] == 1 + 2.0 ** -6), vals
+    assert np.all(vals[0::2] == -(1 + 2.0 ** -6)), vals
+
+
+def test_out_fwd_rounding_point_fp32_modulation(orc):
+    """Worked example of 'the modulation promotes to fp32, one bf16 store'.
+
+    xhat = 0.99999952, onep = 1 (scale 0), shift = 3 * 2^-8: m = 1.0117183 (fp32)
+    lies below the bf16 midpoint 1.01171875, so out = 1 + 2^-7.  Rounding
+    xhat * onep to bf16 first (1.0) would make m = 1.01171875, a tie, and out
+    would be 1 + 2^-6."""
+    D = 8
+    x = _pm_one_row(D).reshape(1, 1, D)
+    emb = np.zeros((1, 2 * D), np.uint16)
+    emb[0, D:] = _bf16(np.full(D, 3 * 2.0 ** -8))
+    out, _, _ = orc.out_fwd(x, emb)
+    vals = bf16_to_f64(out[0, 0])
+    assert np.all(vals[1::2] == 1 + 2.0 ** -7), vals
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm + modulation backward
+# ---------------------------------------------------------------------------
+
+def _torch_out_bwd(dy, x, scale, eps):
+    tx = torch.from_numpy(x).requires_grad_(True)
+    ts = torch.from_numpy(scale).requires_grad_(True)
+    th = torch.zeros_like(ts).requires_grad_(True)
+    D = x.shape[-1]
+    out = torch.nn.functional.layer_norm(tx, (D,), eps=eps) * (1 + ts[:, None, :]) + th[:, None, :]
+    out.backward(torch.from_numpy(dy))
+    return tx.grad.numpy(), ts.grad.numpy(), th.grad.numpy()
+
+
+def test_out_bwd_f64_matches_torch_autograd(orc):
+    rng = np.random.default_rng(9)
+    B, S, D = 2, 6, 48
+    x = rng.standard_normal((B, S, D)) * 2
+    x[0, 3] *= 50
+    scale = rng.standard_normal((B, D)) * 0.2
+    dy = rng.standard_normal((B, S, D))
+    dx, ds, dh = orc.out_bwd_f64(dy, x, scale, 1e-6)
+    rdx, rds, rdh = _torch_out_bwd(dy, x, scale, 1e-6)
+    np.testing.assert_allclose(dx, rdx, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(ds, rds, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dh, rdh, rtol=1e-12, atol=1e-12)
+
+
+def test_out_bwd_f64_finite_differences(orc):
+    rng = np.random.default_rng(10)
+    B, S, D = 1, 3, 8
+    x = rng.standard_normal((B, S, D))
+    scale = rng.standard_normal((B, D)) * 0.3
+    shift = rng.standard_normal((B, D)) * 0.3
+    dy = rng.standard_normal((B, S, D))
+    dx, ds, dh = orc.out_bwd_f64(dy, x, scale, 1e-6)
+    f = lambda xx, sc, sh: float((orc.out_fwd_f64(xx, sc, sh, 1e-6) * dy).sum())
+    h = 1e-6
+    for idx in [(0, 0, 0), (0, 1, 5), (0, 2, 7)]:
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        assert abs((f(xp, scale, shift) - f(xm, scale, shift)) / (2 * h) - dx[idx]) < 1e-6
+    for j in [0, 3, 7]:
+        sp, sm = scale.copy(), scale.copy()
+        sp[0, j] += h
+        sm[0, j] -= h
+        assert abs((f(x, sp, shift) - f(x, sm, shift)) / (2 * h) - ds[0, j]) < 1e-6
+        hp, hm = shift.copy(), shift.copy()
+        hp[0, j] += h
+        hm[0, j] -= h
+        assert abs((f(x, scale, hp) - f(x, scale, hm)) / (2 * h) - dh[0, j]) < 1e-6
+
+
+def test_out_bwd_dx_invariants(orc):
+    """sum_d dx = 0 and sum_d dx * xhat = rstd * D * c2 * eps / (var + eps)
+    (c2 = mean(gh * xhat)), for every row."""
+    rng = np.random.default_rng(11)
+    B, S, D = 1, 4, 128
+    x = rng.standard_normal((B, S, D)) * 0.01  # small variance: eps matters
+    scale = rng.standard_normal((B, D)) * 0.1
+    dy = rng.standard_normal((B, S, D))
+    dx, _, _ = orc.out_bwd_f64(dy, x, scale, 1e-6)
+    mu = x.mean(-1, keepdims=True)
+    var = x.var(-1, keepdims=True)
+    r = 1 / np.sqrt(var + 1e-6)
+    xh = (x - mu) * r
+    gh = dy * (1 + scale[:, None, :])
+    c2 = (gh * xh).mean(-1, keepdims=True)
+    np.testing.assert_allclose(dx.sum(-1), 0, atol=1e-9)
+    np.testing.assert_allclose((dx * xh).sum(-1, keepdims=True), r * D * c2 * 1e-6 / (var + 1e-6), rtol=1e-6, atol=1e-9)
+
+
+def test_out_bwd_token_sums_are_exact(orc):
+    """d_shift = sum_s dy (correctly rounded, math.fsum) and
+    d_scale = sum_s dy * fp32(LN(x)) (correctly rounded), per column."""
+    rng = np.random.default_rng(12)
+    B, S, D = 2, 70, 16
+    x = _bf16(rng.standard_normal((B, S, D)))
+    dy = _bf16(rng.standard_normal((B, S, D)))
+    emb = _bf16(rng.standard_normal((B, 2 * D)) * 0.1)
+    _, d_emb = orc.out_bwd(dy, x, emb)
+    g = bf16_to_f64(dy)
+    xh = torch.nn.functional.layer_norm(torch.from_numpy(bf16_to_f64(x)), (D,), eps=EPS32).numpy().astype(np.float32)
+    for b in range(B):
+        for d in range(D):
+            assert d_emb[b, D + d] == np.float32(math.fsum(g[b, :, d]))
+            assert d_emb[b, d] == np.float32(math.fsum(g[b, :, d] * xh[b, :, d].astype(np.float64)))
+
+
+def test_out_bwd_bf16_entry_rounds_the_f64_gradient(orc):
+    """dx of the bf16 entry is the bf16 rounding of the exact gradient taken at
+    onep = bf16(1 + scale), i.e. with scale' = onep - 1 in the fp64 map."""
+    rng = np.random.default_rng(13)
+    B, S, D = 2, 9, 64
+    x = _bf16(rng.standard_normal((B, S, D)))
+    dy = _bf16(rng.standard_normal((B, S, D)))
+    emb = _bf16(rng.standard_normal((B, 2 * D)) * 0.3)
+    dx, _ = orc.out_bwd(dy, x, emb)
+    onep = bf16_to_f64(synth.bf16_bits_from_f32(np.float32(1) + bf16_to_f64(emb[:, :D]).astype(np.float32)))
+    rdx, _, _ = _torch_out_bwd(bf16_to_f64(dy), bf16_to_f64(x), onep - 1.0, EPS32)
+    assert_bitwise(dx, orc.bf16_from_f64(rdx), "dx = bf16(exact)")
+
+
+# ---------------------------------------------------------------------------
+# token sums
+# ---------------------------------------------------------------------------
+
+def _plain_tree(v):
+    """Uncompensated 32-way tree in fp32 (for the contrast in the worked example)."""
+    v = np.asarray(v, np.float32)
+    while len(v) > 1:
+        n = (len(v) + 31) // 32
+        w = np.concatenate([v, np.zeros(n * 32 - len(v), np.float32)]).reshape(n, 32)
+        s = w[:, 0].copy()
+        for j in range(1, 32):
+            s = (s + w[:, j]).astype(np.float32)
+        v = s
+    return v[0]
+
+
+def test_token_tree_cancellation_worked_example(orc):
+    for S, p, m, want, want_plain in golden_rows("token_tree_cancellation.txt"):
+        S, p, m = int(S), int(p), int(m)
+        a = np.ones((1, S, 1), np.float32)
+        a[0, p, 0] = 2.0 ** 26
+        a[0, m, 0] = -(2.0 ** 26)
+        assert orc.token_tree_f32(a)[0, 0] == float(want), (p, m)
+        assert orc.token_sum_f64(a)[0, 0] == float(want)
+        if int(want_plain) >= 0:
+            assert _plain_tree(a[0, :, 0]) == float(want_plain)
+
+
+def test_token_tree_counts_every_token_once(orc):
+    """Integer-valued inputs whose partial sums stay below 2^24: every fp32
+    operation is exact, so the tree must give the exact sum.  A dropped,
+    repeated or misplaced token, tile or child changes it."""
+    rng = np.random.default_rng(14)
+    for S in [1, 2, 31, 32, 33, 64, 65, 1023, 1024, 1025, 4096, 6032, 6889, 33000]:
+        B, H = 2, 3
+        a = rng.integers(-1000, 1000, size=(B, S, H)).astype(np.float32)
+        a[:, :, 1] = np.arange(S, dtype=np.float32)[None, :] * 0 + (np.arange(S) % 97)[None, :]
+        got = orc.token_tree_f32(a)
+        assert_bitwise(got, a.astype(np.float64).sum(axis=1).astype(np.float32), f"S={S}")
+
+
+def test_token_tree_error_bound_vs_exact(orc):
+    """The compensated tree stays within 2^-23 |sum| + 2^-30 sum|x| of the exact
+    sum (math.fsum) on wide-range random inputs up to S = 40000; a plain fp32
+    tree exceeds that bound on the same inputs."""
+    rng = np.random.default_rng(15)
+    worst_plain = 0.0
+    for S in [33, 1000, 4096, 6889, 40000]:
+        H = 4
+        a = (rng.standard_normal((1, S, H)) * np.exp2(rng.integers(-12, 12, (1, S, H)))).astype(np.float32)
+        got = orc.token_tree_f32(a)[0]
+        for h in range(H):
+            col = a[0, :, h].astype(np.float64)
+            exact = math.fsum(col)
+            bound = 2.0 ** -23 * abs(exact) + 2.0 ** -30 * np.abs(col).sum()
+            assert abs(float(got[h]) - exact) <= bound, (S, h, float(got[h]), exact)
+            worst_plain = max(worst_plain, abs(float(_plain_tree(a[0, :, h])) - exact) / bound)
+    assert worst_plain > 1.0
+
+
+def test_token_tree_small_cases(orc):
+    rng = np.random.default_rng(16)
+    a = rng.standard_normal((3, 1, 5)).astype(np.float32)
+    assert_bitwise(orc.token_tree_f32(a), a[:, 0, :], "S=1 is the identity")
+    a2 = rng.standard_normal((2, 2, 7)).astype(np.float32)
+    assert_bitwise(orc.token_tree_f32(a2), (a2[:, 0] + a2[:, 1]).astype(np.float32), "S=2 is one IEEE add")
+
+
+def test_token_sum_f64_is_correctly_rounded(orc):
+    rng = np.random.default_rng(17)
+    a = (rng.standard_normal((2, 500, 3)) * np.exp2(rng.integers(-20, 20, (2, 500, 3)))).astype(np.float32)
+    got = orc.token_sum_f64(a)
+    for b in range(2):
+        for h in range(3):
+            assert got[b, h] == math.fsum(a[b, :, h].astype(np.float64))
+
+
+def test_bwd_products_reuse_forward_statistics(orc):
+    """prod = (g * fp32(fp32(x - mean) * rstd), g): with mean 0 and rstd 1 the
+    product is g * x exactly; the shift half is g."""
+    rng = np.random.default_rng(18)
+    B, S, D = 1, 3, 8
+    x = _bf16(rng.standard_normal((B, S, D)))
+    dy = _bf16(rng.standard_normal((B, S, D)))
+    p = orc.bwd_products_f32(dy, x, np.zeros((B, S), np.float32), np.ones((B, S), np.float32))
+    assert_bitwise(p[..., :D], (bf16_to_f64(dy) * bf16_to_f64(x)).astype(np.float32), "scale products")
+    assert_bitwise(p[..., D:], bf16_to_f64(dy).astype(np.float32), "shift products")
+
+
+# ---------------------------------------------------------------------------
+# projection backward
+# ---------------------------------------------------------------------------
+
+def test_proj_bwd_f64_matches_torch_autograd(orc):
+    rng = np.random.default_rng(19)
+    B, D = 3, 16
+    temb = rng.standard_normal((B, D))
+    W = rng.standard_normal((2 * D, D)) * 0.2
+    b = rng.standard_normal(2 * D) * 0.2
+    de = rng.standard_normal((B, 2 * D))
+    tt = torch.from_numpy(temb).requires_grad_(True)
+    tW = torch.from_numpy(W).requires_grad_(True)
+    tb = torch.from_numpy(b).requires_grad_(True)
+    torch.nn.functional.linear(torch.nn.functional.silu(tt), tW, tb).backward(torch.from_numpy(de))
+    d_temb, dW, db = orc.proj_bwd_f64(de, temb, W)
+    np.testing.assert_allclose(d_temb, tt.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dW, tW.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(db, tb.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_proj_bwd_bf16_entry(orc):
+    """d_temb = bf16(exact (e @ W) * silu'(t)) with e = bf16(d_emb) (torch fp64
+    autograd of linear(silu)); dW = sum_b e u with u = bf16(silu(t)); B = 1
+    gives dW = e (x) u exactly."""
+    rng = np.random.default_rng(20)
+    B, D = 2, 32
+    temb = _bf16(rng.standard_normal((B, D)))
+    W = _bf16(rng.standard_normal((2 * D, D)) * 0.05)
+    d_emb = rng.standard_normal((B, 2 * D)).astype(np.float32) * 3
+    d_temb, dW, db = orc.proj_bwd(d_emb, temb, W)
+    e = bf16_to_f64(synth.bf16_bits_from_f32(d_emb))
+    tt = torch.from_numpy(bf16_to_f64(temb)).requires_grad_(True)
+    torch.nn.functional.linear(torch.nn.functional.silu(tt), torch.from_numpy(bf16_to_f64(W))).backward(torch.from_numpy(e))
+    assert_bitwise(d_temb, orc.bf16_from_f64(tt.grad.numpy()), "d_temb")
+    u = bf16_to_f64(orc.silu_bf16(temb))
+    np.testing.assert_allclose(dW, e.T @ u, rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(db, e.sum(0))
+    d1, dW1, db1 = orc.proj_bwd(d_emb[:1], temb[:1], W)
+    np.testing.assert_array_equal(dW1, np.outer(e[0], u[0]))
+
+
+def test_wgrad_seq_f32_order_and_chunking(orc):
+    """Sequential fp32 accumulation over samples: B = 1 is the exact outer
+    product; the 5 chunkings of a workload give identical bytes; appended
+    zero samples change nothing; the result is within the sequential-sum
+    bound (B - 1) * 2^-24 * sum|terms| of the fp64 value."""
+    rng = np.random.default_rng(21)
+    B, D = 12, 16
+    temb = _bf16(rng.standard_normal((B, D)))
+    d_emb = rng.standard_normal((B, 2 * D)).astype(np.float32)
+    W = _bf16(rng.standard_normal((2 * D, D)) * 0.05)
+    e = bf16_to_f64(synth.bf16_bits_from_f32(d_emb))
+    u = bf16_to_f64(orc.silu_bf16(temb))
+    dW1, db1 = orc.wgrad_seq_f32(d_emb[:1], temb[:1])
+    assert_bitwise(dW1, np.outer(e[0], u[0]).astype(np.float32), "B=1")
+    full, fullb = orc.wgrad_seq_f32(d_emb, temb)
+    for chunk in [1, 2, 3, 4, 6, 12]:
+        acc, accb = None, None
+        for i in range(0, B, chunk):
+            acc, accb = orc.wgrad_seq_f32(d_emb[i:i + chunk], temb[i:i + chunk], acc, accb, accumulate=acc is not None)
+        assert_bitwise(acc, full, f"chunk {chunk}")
+        assert_bitwise(accb, fullb, f"chunk {chunk} db")
+    pad, padb = orc.wgrad_seq_f32(np.zeros((3, 2 * D), np.float32), temb[:3], full, fullb, accumulate=True)
+    assert_bitwise(pad, full, "zero padding")
+    assert_bitwise(padb, fullb, "zero padding db")
+    _, dW64, db64 = orc.proj_bwd(d_emb, temb, W)
+    bound = (B - 1) * 2.0 ** -24 * (np.abs(e).T @ np.abs(u))
+    assert np.all(np.abs(full - dW64) <= bound + 1e-30)
