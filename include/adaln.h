@@ -1,0 +1,252 @@
+/*
+ * adaln.h — C ABI of libadaln.so: the batch-invariant DiT AdaLN final
+ * modulation ("norm_out"), forward and backward, on NVIDIA GB300 (sm_103a).
+ *
+ * The operator (RL-Kernel PR 538 "final_adaln_out", section "What"):
+ *
+ *     scale, shift = (SiLU(temb) @ W^T + b).chunk(2)      3072 -> 6144, scale first
+ *     out          = LayerNorm(x, eps, no affine) * (1 + scale) + shift
+ *
+ * with the autocast rounding points of miles_diffusion PR 108 ("bitwise
+ * train<->rollout parity ...", Summary, root cause 1): LayerNorm computed and
+ * returned in fp32, (1 + scale) rounded once to bf16, the modulation in fp32,
+ * one bf16 rounding at the store.  The backward returns dx, the token sums
+ * d_scale/d_shift through a fixed 32-way Neumaier tree whose shape depends only
+ * on the sequence length (PR 538, "What" and the review thread on the
+ * cancellation case), and dW, db, d_temb.
+ *
+ * Every result is bitwise independent of the batch size, of the position of a
+ * sample in the batch and (for dW/db) of how samples are split into calls.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are device pointers (memory the current device can read or
+ *    write), each 16-byte aligned.  A pointer may be NULL exactly when its
+ *    buffer has zero bytes (B == 0 or S == 0), and for the optional outputs
+ *    marked "or NULL".  bf16 tensors are passed as their 16-bit
+ *    patterns (adaln_bf16); all tensors are dense, row-major, no strides.
+ *  - The caller owns every buffer, including workspaces.  The library never
+ *    allocates, never frees and never synchronizes: work is enqueued on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
+ *    returns at once.  Kernels may be launched with programmatic dependent
+ *    launch, so a later kernel on the same stream can start its prologue early;
+ *    it still reads results only after this call's kernels have completed.
+ *  - Outputs must not overlap any input, any other output or the workspace
+ *    (ADALN_ERR_ALIAS).  An output is always written, even when it equals an
+ *    input value (S == 1 writes a fresh d_emb; nothing is returned as a view).
+ *  - All arguments are checked on the host before anything is launched, in
+ *    this order: shapes and other argument values, NULL pointers, alignment,
+ *    overlaps, workspace, then the current device (must be compute capability
+ *    10.3).  A failed check
+ *    launches nothing and returns its status.  A failed launch returns
+ *    ADALN_ERR_CUDA; an asynchronous device-side fault surfaces, as for any
+ *    CUDA work, at the caller's next synchronizing CUDA call.
+ *  - Shapes: D % 8 == 0 and 8 <= D <= 8192; 0 <= S <= 262144; B >= 0 with
+ *    B <= 65535 for the token-row calls (adaln_out_*, token_sum_tree) and
+ *    B <= 2^20 for the projection calls; B * S * D < 2^40.  B == 0 or
+ *    S == 0 is valid (see each call).
+ *  - Nothing is thrown across the ABI; no global state changes except the
+ *    device-side error word read by adaln_device_error().
+ */
+#ifndef ADALN_H
+#define ADALN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t adaln_bf16; /* bfloat16 bit pattern */
+
+typedef enum adaln_status {
+    ADALN_OK = 0,
+    ADALN_ERR_NULL = 1,      /* a required pointer is NULL                          */
+    ADALN_ERR_SHAPE = 2,     /* a size is out of range (see the conventions)        */
+    ADALN_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned                    */
+    ADALN_ERR_ALIAS = 4,     /* an output overlaps an input, output or workspace    */
+    ADALN_ERR_WORKSPACE = 5, /* workspace NULL or smaller than the *_workspace_bytes */
+    ADALN_ERR_DEVICE = 6,    /* no current CUDA device, or it is not sm_103         */
+    ADALN_ERR_CUDA = 7,      /* a CUDA runtime call or a kernel launch failed       */
+    ADALN_ERR_ARG = 8        /* another argument is invalid (eps, flag combination) */
+} adaln_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *adaln_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int adaln_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Forward                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * adaln_proj_fwd — modulation projection (PR 538 "What": the (scale, shift)
+ * projection 3072 -> 6144).
+ *
+ *   u[b,k]   = bf16(silu(temb[b,k]))       the bf16 nearest to the fp64 value of
+ *                                          t / (1 + exp(-t))
+ *   emb[b,n] = bf16( sum_k u[b,k] * W[n,k]  +  bias[n] )   fp32 accumulation in a
+ *              fixed order over k, bias added in fp32, one bf16 rounding
+ *
+ *   temb [B, D]    bf16   conditioning vector
+ *   W    [2D, D]   bf16   row n = output feature n; rows 0..D-1 give scale,
+ *                         rows D..2D-1 give shift
+ *   bias [2D]      bf16
+ *   emb  [B, 2D]   bf16   output, [scale | shift] per sample
+ *   u    [B, D]    bf16   output, the SiLU activation (the projection's input,
+ *                         saved for adaln_proj_bwd)
+ *
+ * The k-order of every dot product is fixed by D alone, so emb[b,:] does not
+ * depend on B or on b.  B == 0 launches nothing.
+ */
+adaln_status adaln_proj_fwd(const adaln_bf16 *temb, const adaln_bf16 *W, const adaln_bf16 *bias,
+                            adaln_bf16 *emb, adaln_bf16 *u, int B, int D, void *stream);
+
+/*
+ * adaln_out_fwd — LayerNorm (no affine) + modulation (PR 538 "What"; rounding
+ * points of PR 108 Summary, root cause 1).
+ *
+ *   per token row r = (b, s), over d in [0, D):
+ *     mean[r] = fp32 sum_d x / D                    fixed-order fp32 reductions
+ *     rstd[r] = 1 / sqrt(sum_d (x - mean)^2 / D + eps)   (biased variance)
+ *     xhat    = fp32(fp32(x - mean) * rstd)
+ *     onep    = bf16(fp32(1 + scale[b,d]))          scale = emb[b, 0:D]
+ *     out     = bf16( fp32( fp32(xhat * onep) + shift[b,d] ) )   shift = emb[b, D:2D]
+ *
+ *   x    [B, S, D] bf16    input tokens
+ *   emb  [B, 2D]   bf16    from adaln_proj_fwd
+ *   out  [B, S, D] bf16    output
+ *   mean [B, S]    fp32    output, saved for the backward
+ *   rstd [B, S]    fp32    output, saved for the backward
+ *   eps            fp32    LayerNorm epsilon (1e-6 in the model), finite, >= 0
+ *
+ * The reduction order over d depends only on D; rows never interact.
+ * B * S == 0 launches nothing.
+ */
+adaln_status adaln_out_fwd(const adaln_bf16 *x, const adaln_bf16 *emb, adaln_bf16 *out,
+                           float *mean, float *rstd, int B, int S, int D, float eps, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Backward                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes adaln_out_bwd needs: the level-0 token-tree partials,
+ * 2 * B * ceil(S/32) * 2D fp32 values, rounded up to 256 bytes.  0 if B*S == 0. */
+size_t adaln_out_bwd_workspace_bytes(int B, int S, int D);
+
+/*
+ * adaln_out_bwd — backward of adaln_out_fwd for the upstream gradient dy
+ * (PR 538 "What": LayerNorm backward per row; d_scale, d_shift as token sums
+ * in the fixed 32-way tree).
+ *
+ *   g     = fp32(dy);  gh = g * onep (exact);  xhat as in the forward, from the
+ *           saved mean/rstd, bit-identical to the forward's value
+ *   dx    = bf16( rstd * ((gh - c1) - xhat * c2) ),  c1 = sum_d gh / D,
+ *           c2 = sum_d gh*xhat / D   (fixed-order fp32 reductions over d)
+ *   d_emb[b, 0:D]  = d_scale = tree_s( fp32(g * xhat) )
+ *   d_emb[b, D:2D] = d_shift = tree_s( g )
+ *
+ *   tree_s: the fixed 32-way tree over s = 0..S-1.  Level 0 cuts the tokens
+ *   into tiles of 32 (the last may be short); each tile is a Neumaier sum in
+ *   ascending order starting from its first token, giving (sum, correction).
+ *   Each further level cuts the nodes into groups of 32 (the last may be
+ *   short); a group's sum is the Neumaier sum of its children's sums in
+ *   ascending order, and its correction is that sum's compensation plus the
+ *   children's corrections added in ascending order.  The root is the first
+ *   level with one node; the result is sum + correction (one IEEE add).  The
+ *   shape depends on S only.  Neumaier step: t = s + v; if |s| >= |v| then
+ *   c += (s - t) + v else c += (v - t) + s; s = t.
+ *
+ *   dy, x     [B, S, D] bf16     inputs
+ *   emb       [B, 2D]   bf16     input (as given to the forward)
+ *   mean,rstd [B, S]    fp32     inputs, from adaln_out_fwd
+ *   dx        [B, S, D] bf16     output
+ *   d_emb     [B, 2D]   fp32     output, [d_scale | d_shift]
+ *   workspace                    >= adaln_out_bwd_workspace_bytes(B, S, D)
+ *
+ * S == 0 writes d_emb = +0; B == 0 launches nothing.
+ */
+adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb,
+                           const float *mean, const float *rstd, adaln_bf16 *dx, float *d_emb,
+                           void *workspace, size_t workspace_bytes, int B, int S, int D, void *stream);
+
+/* Workspace bytes token_sum_tree needs: 2 * B * ceil(S/32) * H fp32 values,
+ * rounded up to 256 bytes.  0 if B*S == 0. */
+size_t token_sum_tree_workspace_bytes(int B, int S, int H);
+
+/*
+ * token_sum_tree — the fixed 32-way token tree on its own (PR 538 "What":
+ * the FP32 token-sum kernel; review thread on the cancellation case).
+ *
+ *   out[b,h] = tree_s(in[b,s,h]), the tree defined under adaln_out_bwd.
+ *
+ *   in  [B, S, H] fp32   H % 4 == 0, 4 <= H <= 2^20
+ *   out [B, H]    fp32   output (a fresh buffer, also when S == 1)
+ *
+ * On the same values it returns the same bytes as the d_emb of
+ * adaln_out_bwd.  S == 0 writes out = +0; B == 0 launches nothing.
+ */
+adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes adaln_proj_bwd needs: the per-slab d_silu partials,
+ * ceil(2D/384) * B * D fp32 values, rounded up to 256 bytes. */
+size_t adaln_proj_bwd_workspace_bytes(int B, int D);
+
+/*
+ * adaln_proj_bwd — backward of adaln_proj_fwd (PR 538 "What": the projection
+ * backward of the reused fixed-order projection; the SiLU VJP as in the review
+ * finding on the analytic SiLU derivative).
+ *
+ *   e[b,n]      = bf16(d_emb[b,n])        (emb is a bf16 tensor)
+ *   d_temb[b,k] = bf16( (sum_n e[b,n] W[n,k]) * sigma(t) (1 + t (1 - sigma(t))) ),
+ *                 t = temb[b,k]; fp32 sum whose n-order is fixed by D alone
+ *   dW[n,k]     : acc = accumulate ? dW_acc[n,k] : +0;
+ *                 for b = 0 .. B-1 (ascending): acc = acc + e[b,n] * u[b,k]
+ *                 (the product is exact in fp32; one rounding per add)
+ *   db[n]       : the same with e[b,n] alone
+ *
+ *   d_emb  [B, 2D] fp32   input (from adaln_out_bwd)
+ *   temb   [B, D]  bf16   input
+ *   u      [B, D]  bf16   input, the SiLU activation from adaln_proj_fwd
+ *   W      [2D, D] bf16   input
+ *   d_temb [B, D]  bf16   output
+ *   dW_acc [2D, D] fp32   in/out accumulator, or NULL
+ *   db_acc [2D]    fp32   in/out accumulator, or NULL
+ *   dW     [2D, D] bf16   output bf16(acc), or NULL
+ *   db     [2D]    bf16   output bf16(acc), or NULL
+ *   accumulate            0: start from +0; 1: start from dW_acc/db_acc (which
+ *                         must then be non-NULL for every gradient computed)
+ *   workspace             >= adaln_proj_bwd_workspace_bytes(B, D)
+ *
+ * The weight gradient is computed when dW_acc or dW is non-NULL, the bias
+ * gradient when db_acc or db is non-NULL.  Calling with samples 0..k-1 and
+ * then, with accumulate = 1, samples k..B-1 gives the same bytes as one call
+ * with all B samples.  B == 0 with accumulate = 0 writes zeros.
+ */
+adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const adaln_bf16 *u,
+                            const adaln_bf16 *W, adaln_bf16 *d_temb, float *dW_acc, float *db_acc,
+                            adaln_bf16 *dW, adaln_bf16 *db, int accumulate,
+                            void *workspace, size_t workspace_bytes, int B, int D, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * adaln_device_error — reads and clears the device-side error word of the
+ * current device (synchronizes the device).  Kernels that wait on their own
+ * asynchronous copies give each wait a time limit; a wait that runs out sets
+ * this word (non-zero: the kernel code) instead of hanging, and the kernel
+ * returns without finishing its outputs.  Returns 0 when no kernel failed,
+ * -1 if the word could not be read.
+ */
+int adaln_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADALN_H */

@@ -1,0 +1,270 @@
+// C ABI of libadaln.so (declared in include/adaln.h): host-side argument
+// checks, then the launches.  Every check runs before anything is enqueued;
+// the order is shapes and argument values, NULL pointers (a pointer may be
+// NULL only when its buffer has zero bytes), alignment, overlaps, workspace
+// size, current device.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "adaln.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace adaln {
+
+namespace {
+
+struct Buf {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlaps(const Buf &a, const Buf &b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Every output against every input, every other output and the workspace.
+bool any_alias(const Buf *outs, int nout, const Buf *ins, int nin) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlaps(outs[i], ins[j])) return true;
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j])) return true;
+    }
+    return false;
+}
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+// a buffer with bytes > 0 needs a pointer
+bool missing(const Buf &b) { return b.bytes > 0 && b.p == nullptr; }
+bool any_missing(const Buf *bufs, int n) {
+    for (int i = 0; i < n; ++i)
+        if (missing(bufs[i])) return true;
+    return false;
+}
+
+bool valid_D(int D) { return D >= 8 && D <= kMaxD && D % 8 == 0; }
+
+bool valid_BS(int B, int S, int D) {
+    if (B < 0 || S < 0 || S > kMaxS || B > 65535) return false;
+    return (long double)B * S * D < 1099511627776.0L;  // 2^40
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+std::mutex g_mu;
+
+// Current device, its SM count and compute capability, cached per device.
+adaln_status current_device(DeviceInfo *info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ADALN_ERR_DEVICE;
+    }
+    static std::unordered_map<int, DeviceInfo> cache;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cache.find(dev);
+        if (it != cache.end()) {
+            *info = it->second;
+            return (info->cc_major == 10 && info->cc_minor == 3) ? ADALN_OK : ADALN_ERR_DEVICE;
+        }
+    }
+    DeviceInfo d{dev, 0, 0, 0};
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ADALN_ERR_DEVICE;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cache[dev] = d;
+    }
+    *info = d;
+    return (d.cc_major == 10 && d.cc_minor == 3) ? ADALN_OK : ADALN_ERR_DEVICE;
+}
+
+adaln_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return ADALN_OK;
+    cudaGetLastError();  // clear a non-sticky launch error
+    return ADALN_ERR_CUDA;
+}
+
+size_t tiles(int S) { return (size_t)((S + kTile - 1) / kTile); }
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &dev) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static std::unordered_map<const void *, size_t> done[64];
+    const int slot = dev.device & 63;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = done[slot].find(func);
+        if (it != done[slot].end() && it->second >= bytes) return cudaSuccess;
+    }
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        size_t &v = done[slot][func];
+        if (bytes > v) v = bytes;
+    }
+    return e;
+}
+
+}  // namespace adaln
+
+using namespace adaln;
+
+extern "C" {
+
+const char *adaln_status_string(int status) {
+    switch (status) {
+        case ADALN_OK: return "ADALN_OK";
+        case ADALN_ERR_NULL: return "ADALN_ERR_NULL: a required pointer is NULL";
+        case ADALN_ERR_SHAPE: return "ADALN_ERR_SHAPE: a size is out of range";
+        case ADALN_ERR_ALIGN: return "ADALN_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case ADALN_ERR_ALIAS: return "ADALN_ERR_ALIAS: an output overlaps an input, another output or the workspace";
+        case ADALN_ERR_WORKSPACE: return "ADALN_ERR_WORKSPACE: workspace missing or too small";
+        case ADALN_ERR_DEVICE: return "ADALN_ERR_DEVICE: no current CUDA device, or it is not compute capability 10.3";
+        case ADALN_ERR_CUDA: return "ADALN_ERR_CUDA: a CUDA call or kernel launch failed";
+        case ADALN_ERR_ARG: return "ADALN_ERR_ARG: an argument value is invalid";
+        default: return "unknown adaln status";
+    }
+}
+
+int adaln_version(void) { return (1 << 16) | 0; }
+
+size_t adaln_out_bwd_workspace_bytes(int B, int S, int D) {
+    if (B <= 0 || S <= 0 || D <= 0) return 0;
+    return round256(2 * (size_t)B * tiles(S) * 2 * (size_t)D * sizeof(float));
+}
+
+size_t token_sum_tree_workspace_bytes(int B, int S, int H) {
+    if (B <= 0 || S <= 0 || H <= 0) return 0;
+    return round256(2 * (size_t)B * tiles(S) * (size_t)H * sizeof(float));
+}
+
+size_t adaln_proj_bwd_workspace_bytes(int B, int D) {
+    if (B <= 0 || D <= 0) return 0;
+    const size_t nslab = (size_t)(2 * D + kProjSlabRows - 1) / kProjSlabRows;
+    return round256(nslab * (size_t)B * D * sizeof(float));
+}
+
+adaln_status adaln_proj_fwd(const adaln_bf16 *temb, const adaln_bf16 *W, const adaln_bf16 *bias, adaln_bf16 *emb,
+                            adaln_bf16 *u, int B, int D, void *stream) {
+    if (!valid_D(D) || B < 0 || B > (1 << 20)) return ADALN_ERR_SHAPE;
+    const size_t N = 2 * (size_t)D;
+    const Buf ins[] = {{temb, (size_t)B * D * 2}, {W, N * D * 2}, {bias, N * 2}};
+    const Buf outs[] = {{emb, (size_t)B * N * 2}, {u, (size_t)B * D * 2}};
+    if (any_missing(ins, 3) || any_missing(outs, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(temb) || !aligned16(W) || !aligned16(bias) || !aligned16(emb) || !aligned16(u))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 2, ins, 3)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_proj_fwd(temb, W, bias, emb, u, B, D, (cudaStream_t)stream, dev));
+}
+
+adaln_status adaln_out_fwd(const adaln_bf16 *x, const adaln_bf16 *emb, adaln_bf16 *out, float *mean, float *rstd,
+                           int B, int S, int D, float eps, void *stream) {
+    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return ADALN_ERR_ARG;
+    const size_t rows = (size_t)B * S;
+    const Buf ins[] = {{x, rows * D * 2}, {emb, (size_t)B * 2 * D * 2}};
+    const Buf outs[] = {{out, rows * D * 2}, {mean, rows * 4}, {rstd, rows * 4}};
+    if (any_missing(ins, 2) || any_missing(outs, 3)) return ADALN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(emb) || !aligned16(out) || !aligned16(mean) || !aligned16(rstd))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 3, ins, 2)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (rows == 0) return ADALN_OK;
+    return from_cuda(launch_out_fwd(x, emb, out, mean, rstd, B, S, D, eps, (cudaStream_t)stream, dev));
+}
+
+adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb, const float *mean,
+                           const float *rstd, adaln_bf16 *dx, float *d_emb, void *workspace, size_t workspace_bytes,
+                           int B, int S, int D, void *stream) {
+    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    const size_t rows = (size_t)B * S;
+    const size_t need = adaln_out_bwd_workspace_bytes(B, S, D);
+    const Buf ins[] = {{dy, rows * D * 2}, {x, rows * D * 2}, {emb, (size_t)B * 2 * D * 2}, {mean, rows * 4},
+                       {rstd, rows * 4}};
+    const Buf outs[] = {{dx, rows * D * 2}, {d_emb, (size_t)B * 2 * D * 4}, {workspace, need}};
+    if (any_missing(ins, 5) || any_missing(outs, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(emb) || !aligned16(mean) || !aligned16(rstd) ||
+        !aligned16(dx) || !aligned16(d_emb) || !aligned16(workspace))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 3, ins, 5)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_out_bwd(dy, x, emb, mean, rstd, dx, d_emb, workspace, B, S, D, (cudaStream_t)stream, dev));
+}
+
+adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    if (H < 4 || H > (1 << 20) || H % 4 != 0 || B < 0 || B > 65535 || S < 0 || S > kMaxS ||
+        (long double)B * S * H >= 1099511627776.0L)
+        return ADALN_ERR_SHAPE;
+    const size_t need = token_sum_tree_workspace_bytes(B, S, H);
+    const Buf ins[] = {{in, (size_t)B * S * H * 4}};
+    const Buf outs[] = {{out, (size_t)B * H * 4}, {workspace, need}};
+    if (any_missing(ins, 1) || any_missing(outs, 1)) return ADALN_ERR_NULL;
+    if (!aligned16(in) || !aligned16(out) || !aligned16(workspace)) return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 2, ins, 1)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_token_tree(in, out, workspace, B, S, H, (cudaStream_t)stream, dev));
+}
+
+adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const adaln_bf16 *u, const adaln_bf16 *W,
+                            adaln_bf16 *d_temb, float *dW_acc, float *db_acc, adaln_bf16 *dW, adaln_bf16 *db,
+                            int accumulate, void *workspace, size_t workspace_bytes, int B, int D, void *stream) {
+    if (!valid_D(D) || B < 0 || B > (1 << 20)) return ADALN_ERR_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return ADALN_ERR_ARG;
+    const bool want_w = dW_acc || dW, want_b = db_acc || db;
+    if (accumulate && ((want_w && !dW_acc) || (want_b && !db_acc))) return ADALN_ERR_ARG;
+    const size_t N = 2 * (size_t)D;
+    const size_t need = adaln_proj_bwd_workspace_bytes(B, D);
+    const Buf ins[] = {{d_emb, (size_t)B * N * 4}, {temb, (size_t)B * D * 2}, {u, (size_t)B * D * 2},
+                       {W, B > 0 ? N * D * 2 : 0}};
+    // dW_acc / db_acc are read as well as written: they count as outputs here
+    const Buf outs[] = {{d_temb, (size_t)B * D * 2}, {dW_acc, N * D * 4}, {db_acc, N * 4}, {dW, N * D * 2},
+                        {db, N * 2}, {workspace, need}};
+    if (any_missing(ins, 4) || missing(outs[0])) return ADALN_ERR_NULL;
+    if (!aligned16(d_emb) || !aligned16(temb) || !aligned16(u) || !aligned16(W) || !aligned16(d_temb) ||
+        !aligned16(dW_acc) || !aligned16(db_acc) || !aligned16(dW) || !aligned16(db) || !aligned16(workspace))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 6, ins, 4)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0 && !want_w && !want_b) return ADALN_OK;
+    return from_cuda(launch_proj_bwd(d_emb, temb, u, W, d_temb, dW_acc, db_acc, dW, db, accumulate, workspace, B, D,
+                                     (cudaStream_t)stream, dev));
+}
+
+int adaln_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    return read_and_clear_device_error();
+}
+
+}  // extern "C"

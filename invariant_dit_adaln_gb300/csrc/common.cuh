@@ -1,0 +1,183 @@
+// Device helpers shared by the kernels of libadaln.so (sm_103a only).
+//
+// Numerics: the library is compiled with --fmad=false and without fast math;
+// every rounding point of the operator is written with an explicit
+// round-to-nearest intrinsic (__fadd_rn, __fmul_rn, ...), so no contraction
+// or reassociation can change a result.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace adaln {
+
+// --------------------------------------------------------------------------
+// limits shared by the host checks and the kernels
+// --------------------------------------------------------------------------
+constexpr int kMaxD = 8192;
+constexpr int kMaxS = 262144;           // 32^3 * 8 tokens: at most 256 level-1 nodes
+constexpr int kTile = 32;               // the token tree's fan-out
+constexpr int kMaxLevel1 = kMaxS / (kTile * kTile);  // 256
+constexpr int kProjSlabRows = 384;      // rows of W per d_silu partial (fixed by D only)
+constexpr int kProjKChunk = 256;        // columns of W per projection-backward CTA
+
+// Error word (device side) set by a wait that ran out of time.
+enum DeviceError : unsigned {
+    kErrNone = 0,
+    kErrOutFwdWait = 0x101,
+    kErrOutBwdWait = 0x201,
+};
+
+// --------------------------------------------------------------------------
+// bf16
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// two floats -> packed bf16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// unpack 8 bf16 (one 16-byte vector) into floats
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// --------------------------------------------------------------------------
+// SiLU rounded to bf16: the nearest bf16 to the fp64 value of t/(1+exp(-t)).
+// Computed in fp32 (error below 4 fp32 ulps); when the fp32 value lies within
+// 16 fp32 ulps of a bf16 rounding midpoint, or exp(-t) would overflow fp32,
+// it is recomputed in fp64 and rounded once from fp64.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t silu_bf16(uint16_t tb) {
+    const float t = bf16f(tb);
+    const float den = __fadd_rn(1.0f, expf(-t));
+    const float s = __fdiv_rn(t, den);
+    const int low = (int)(__float_as_uint(s) & 0xFFFFu) - 0x8000;
+    if (t < -80.0f || (low <= 16 && low >= -16)) {
+        const double td = (double)t;
+        const double sd = td / (1.0 + exp(-td));
+        return __bfloat16_as_ushort(__double2bfloat16(sd));
+    }
+    return bf16_bits(s);
+}
+
+// SiLU derivative sigma(t) * (1 + t * (1 - sigma(t))) in fp32
+__device__ __forceinline__ float dsilu_f32(float t) {
+    const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-t)));
+    return __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(t, __fsub_rn(1.0f, sg))));
+}
+
+// --------------------------------------------------------------------------
+// Neumaier step (the operator's token tree): t = s + v; the part of the
+// smaller operand lost in t is added to c; |s| == |v| takes the first branch.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void neumaier(float &s, float &c, float v) {
+    const float t = __fadd_rn(s, v);
+    const float lost = (fabsf(s) >= fabsf(v)) ? __fadd_rn(__fsub_rn(s, t), v)
+                                              : __fadd_rn(__fsub_rn(v, t), s);
+    c = __fadd_rn(c, lost);
+    s = t;
+}
+
+// --------------------------------------------------------------------------
+// warp reductions with a fixed butterfly; every lane ends with the same bits
+// (each pairwise add is commutative, so partners compute identical values).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    return v;
+}
+
+// --------------------------------------------------------------------------
+// shared memory, mbarriers, bulk copies (the TMA engine), PDL
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// make barrier initialisation visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for a phase of an mbarrier, for at most `limit_ns` nanoseconds.
+// Returns false when the time ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// named barrier over `count` threads (a multiple of 32)
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion
+// (and the visibility of its writes); allow the next grid to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 16-byte global loads/stores
+__device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void stg16(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
+__device__ __forceinline__ void stg16f(void *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+}  // namespace adaln

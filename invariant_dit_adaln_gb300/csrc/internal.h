@@ -1,0 +1,57 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel
+// translation units (out.cu, proj.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace adaln {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major;
+    int cc_minor;
+};
+
+// Raise the dynamic shared-memory limit of a kernel once per (kernel, device).
+cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &dev);
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the preceding kernel on the stream finishes; every kernel of this
+// library calls griddepcontrol.wait before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// out.cu
+cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean, float *rstd,
+                           int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
+                           const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
+                           cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_token_tree(const float *in, float *out, void *ws, int B, int S, int H, cudaStream_t stream,
+                              const DeviceInfo &dev);
+int read_and_clear_device_error();
+
+// proj.cu
+cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
+                            uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
+                            uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
+                            int accumulate, void *ws, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
+
+}  // namespace adaln

@@ -1,0 +1,433 @@
+// Modulation projection 3072 -> 6144 (forward and backward).
+//
+// Operator: RL-Kernel PR 538 "final_adaln_out", section "What": scale, shift =
+// (SiLU(temb) @ W^T + b).chunk(2), computed by a fixed-order projection and
+// its backward.  At the batch sizes of a diffusion step (B = 1, 2) the work is
+// weight-bandwidth bound (37.7 MB of W against B * 37.7 MFLOP), so every
+// kernel here streams W once per call on CUDA cores, with an accumulation
+// order that depends only on D, never on B or on a sample's position.
+//
+// Layout: W [2D, D] bf16 row-major (row n = output feature n), temb, u [B, D]
+// bf16, emb [B, 2D] bf16, d_emb [B, 2D] fp32, dW [2D, D], db [2D].
+#include "common.cuh"
+#include "internal.h"
+
+namespace adaln {
+
+// --------------------------------------------------------------------------
+// u = bf16(silu(temb)): 8 elements per thread
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) silu_kernel(const uint16_t *__restrict__ temb, uint16_t *__restrict__ u,
+                                                   long long n8) {
+    pdl_wait();
+    pdl_trigger();  // the next kernel (the projection) reads u only after its own wait
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint4 t = ldg16(temb + i * 8);
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = silu_bf16((uint16_t)(w[q] & 0xFFFFu));
+        const uint16_t hi = silu_bf16((uint16_t)(w[q] >> 16));
+        o[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    stg16(u + i * 8, make_uint4(o[0], o[1], o[2], o[3]));
+}
+
+// --------------------------------------------------------------------------
+// emb[b,n] = bf16(sum_k u[b,k] W[n,k] + bias[n]).  One warp per output row n.
+// Lane l accumulates the 16-byte vectors v = l, l+32, l+64, ... of the row in
+// ascending order (8 products each, in element order; each product of two
+// bf16 is exact in fp32, so the fused multiply-add rounds once per term), then
+// the lanes combine by a fixed xor butterfly.  The samples are staged in
+// shared memory BC at a time; the order per (b, n) never changes.
+// --------------------------------------------------------------------------
+constexpr int kFwdVL = 12;  // W vectors per lane held in registers (one row of D = 3072)
+
+template <int BC>
+__global__ void __launch_bounds__(256, 3)
+proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias, const uint16_t *__restrict__ u,
+                uint16_t *__restrict__ emb, int B, int D) {
+    extern __shared__ __align__(128) uint4 us[];  // [BC][D/8]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = 2 * D;
+    const int V = D >> 3;
+    const int n = blockIdx.x * 8 + warp;
+    const bool live = n < N;
+    const uint16_t *wrow = W + (size_t)(live ? n : N - 1) * D;
+    const bool one_chunk = V <= 32 * kFwdVL;
+
+    // W and bias are inputs of this call, never outputs of the kernel that
+    // precedes this one (the SiLU kernel above), so they are read before the wait.
+    uint4 wv[kFwdVL];
+#pragma unroll
+    for (int q = 0; q < kFwdVL; ++q) {
+        const int v = lane + 32 * q;
+        if (v < V) wv[q] = ldg16(wrow + (size_t)v * 8);
+    }
+    const float bn = bf16f(bias[live ? n : N - 1]);
+    pdl_wait();
+
+    for (int b0 = 0; b0 < B; b0 += BC) {
+        const int nb = min(BC, B - b0);
+        for (int i = threadIdx.x; i < nb * V; i += blockDim.x) us[i] = ldg16(u + (size_t)b0 * D + (size_t)i * 8);
+        __syncthreads();
+        float acc[BC];
+#pragma unroll
+        for (int b = 0; b < BC; ++b) acc[b] = 0.0f;
+        for (int v0 = 0; v0 < V; v0 += 32 * kFwdVL) {
+            if (!one_chunk && (v0 > 0 || b0 > 0)) {
+#pragma unroll
+                for (int q = 0; q < kFwdVL; ++q) {
+                    const int v = v0 + lane + 32 * q;
+                    if (v < V) wv[q] = ldg16(wrow + (size_t)v * 8);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kFwdVL; ++q) {
+                const int v = v0 + lane + 32 * q;
+                if (v < V) {
+                    float w[8];
+                    unpack8(wv[q], w);
+#pragma unroll
+                    for (int b = 0; b < BC; ++b) {
+                        if (b < nb) {
+                            float x[8];
+                            unpack8(us[b * V + v], x);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[b] = __fmaf_rn(x[e], w[e], acc[b]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BC; ++b) {
+            if (b < nb) {
+                const float tot = warp_sum(acc[b]);
+                if (lane == 0 && live) emb[(size_t)(b0 + b) * N + n] = bf16_bits(__fadd_rn(tot, bn));
+            }
+        }
+        __syncthreads();
+    }
+    pdl_trigger();
+}
+
+// --------------------------------------------------------------------------
+// Backward, kernel 1: one CTA per (k-chunk of 256 columns, slab of 384 rows).
+//
+// Warp w takes the slab's rows n = n0 + w + 8 i (i ascending), lane l the 8
+// columns k = k0 + 8 l .. +7.  For the samples of the current chunk it adds
+// e[b,n] * W[n,k] into fp32 partials (each product exact), then the 8 warps'
+// partials are added in ascending warp order and written per slab:
+// ws[slab][b][k].  The slab size, and so this order, depends on D only.
+// With WITH_W (all samples in one chunk) it also produces dW and db for its
+// tile: acc = (accumulate ? acc_in : +0), then + e[b,n] * u[b,k] for b
+// ascending, one rounding per add.
+// --------------------------------------------------------------------------
+constexpr int kSlabRows = kProjSlabRows;        // 384
+constexpr int kRowsPerWarp = kSlabRows / 8;     // 48
+constexpr int kPre = 4;                         // rows loaded ahead per warp
+
+template <int BC>
+struct SlabSmem {
+    float es[BC][kSlabRows];
+    float red[8][BC][kProjKChunk];
+};
+
+template <int BC, bool WITH_W>
+__global__ void __launch_bounds__(256)
+proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, const uint16_t *__restrict__ W,
+                     float *__restrict__ dW_acc, float *__restrict__ db_acc, uint16_t *__restrict__ dW,
+                     uint16_t *__restrict__ db, int accumulate, float *__restrict__ ws, int B, int D) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    SlabSmem<BC> &sm = *reinterpret_cast<SlabSmem<BC> *>(smem_raw);
+    const int kchunk = blockIdx.x;
+    const int slab = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = 2 * D;
+    const int V = D >> 3;
+    const int n0 = slab * kSlabRows;
+    const int kv = kchunk * 32 + lane;
+    const bool live_k = kv < V;
+    const int col = kv * 8;
+    const int cnt = min(kRowsPerWarp, (N - n0) / 8);  // rows per warp, equal for all warps
+    const bool want_dw = WITH_W && (dW_acc != nullptr || dW != nullptr);
+    const bool want_db = WITH_W && (db_acc != nullptr || db != nullptr) && kchunk == 0 && lane == 0;
+
+    pdl_wait();
+
+    for (int b0 = 0; b0 < B || (WITH_W && b0 == 0); b0 += BC) {
+        const int nb = max(0, min(BC, B - b0));
+        for (int i = threadIdx.x; i < BC * kSlabRows; i += blockDim.x) {
+            const int b = i / kSlabRows, r = i % kSlabRows;
+            const int n = n0 + r;
+            sm.es[b][r] = (b < nb && n < N) ? bf16f(bf16_bits(d_emb[(size_t)(b0 + b) * N + n])) : 0.0f;
+        }
+        float uf[BC][8];
+#pragma unroll
+        for (int b = 0; b < BC; ++b) {
+            if (WITH_W && b < nb && live_k) {
+                unpack8(ldg16(u + (size_t)(b0 + b) * D + col), uf[b]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) uf[b][q] = 0.0f;
+            }
+        }
+        __syncthreads();
+
+        float ds[BC][8];
+#pragma unroll
+        for (int b = 0; b < BC; ++b)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ds[b][q] = 0.0f;
+
+        for (int i0 = 0; i0 < cnt; i0 += kPre) {
+            uint4 wv[kPre];
+#pragma unroll
+            for (int p = 0; p < kPre; ++p) {
+                const int n = n0 + warp + 8 * (i0 + p);
+                if (i0 + p < cnt && live_k && nb > 0) wv[p] = ldg16(W + (size_t)n * D + col);
+            }
+#pragma unroll
+            for (int p = 0; p < kPre; ++p) {
+                const int i = i0 + p;
+                if (i < cnt && live_k) {
+                    const int r = warp + 8 * i;
+                    const int n = n0 + r;
+                    float w[8];
+                    unpack8(nb > 0 ? wv[p] : make_uint4(0u, 0u, 0u, 0u), w);  // W is not read without samples
+#pragma unroll
+                    for (int b = 0; b < BC; ++b) {
+                        if (b < nb) {
+                            const float e = sm.es[b][r];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) ds[b][q] = __fmaf_rn(e, w[q], ds[b][q]);
+                        }
+                    }
+                    if (want_dw) {
+                        float acc[8];
+                        float *pa = dW_acc ? dW_acc + (size_t)n * D + col : nullptr;
+                        if (accumulate) {
+                            const float4 a0 = *reinterpret_cast<const float4 *>(pa);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(pa + 4);
+                            acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
+                            acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                        }
+#pragma unroll
+                        for (int b = 0; b < BC; ++b) {
+                            if (b < nb) {
+                                const float e = sm.es[b][r];
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(e, uf[b][q], acc[q]);
+                            }
+                        }
+                        if (pa) {
+                            stg16f(pa, make_float4(acc[0], acc[1], acc[2], acc[3]));
+                            stg16f(pa + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+                        }
+                        if (dW) stg16(dW + (size_t)n * D + col, pack8(acc));
+                    }
+                }
+                if (want_db && i < cnt) {
+                    const int r = warp + 8 * i;
+                    const int n = n0 + r;
+                    float a = accumulate ? db_acc[n] : 0.0f;
+                    for (int b = 0; b < nb; ++b) a = __fadd_rn(a, sm.es[b][r]);
+                    if (db_acc) db_acc[n] = a;
+                    if (db) db[n] = bf16_bits(a);
+                }
+            }
+        }
+        // the slab's partial d_silu: warps added in ascending order
+#pragma unroll
+        for (int b = 0; b < BC; ++b)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sm.red[warp][b][lane * 8 + q] = ds[b][q];
+        __syncthreads();
+        for (int i = threadIdx.x; i < nb * kProjKChunk; i += blockDim.x) {
+            const int b = i / kProjKChunk, c = i % kProjKChunk;
+            const int k = kchunk * kProjKChunk + c;
+            if (k < D) {
+                float tot = sm.red[0][b][c];
+#pragma unroll
+                for (int w = 1; w < 8; ++w) tot = __fadd_rn(tot, sm.red[w][b][c]);
+                ws[((size_t)slab * B + b0 + b) * D + k] = tot;
+            }
+        }
+        __syncthreads();
+    }
+    pdl_trigger();
+}
+
+// --------------------------------------------------------------------------
+// Backward, kernel 2: d_temb[b,k] = bf16((sum over slabs, ascending) * silu'(t))
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__ temb, uint16_t *__restrict__ d_temb,
+                      int B, int D, int nslab) {
+    pdl_wait();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long BD = (long long)B * D;
+    if (i < BD) {
+        float tot = ws[i];
+        for (int s = 1; s < nslab; ++s) tot = __fadd_rn(tot, ws[(size_t)s * BD + i]);
+        d_temb[i] = bf16_bits(__fmul_rn(tot, dsilu_f32(bf16f(temb[i]))));
+    }
+    pdl_trigger();
+}
+
+// --------------------------------------------------------------------------
+// dW / db for many samples: a 64 x 64 tile of dW per CTA, thread (tn, tk)
+// owning rows n0 + 4 tn .. +3 and columns k0 + 4 tk .. +3; samples stream
+// through shared memory 32 at a time and are added in ascending order,
+// exactly as in the slab kernel: acc = acc + e[b,n] * u[b,k].
+// --------------------------------------------------------------------------
+constexpr int kDwTile = 64;
+constexpr int kDwBChunk = 32;
+
+__global__ void __launch_bounds__(256)
+proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, float *__restrict__ dW_acc,
+                     uint16_t *__restrict__ dW, int accumulate, int B, int D) {
+    __shared__ __align__(16) float es[kDwBChunk][kDwTile];
+    __shared__ __align__(16) float us[kDwBChunk][kDwTile];
+    const int N = 2 * D;
+    const int k0 = blockIdx.x * kDwTile;
+    const int n0 = blockIdx.y * kDwTile;
+    const int tk = threadIdx.x & 15;
+    const int tn = threadIdx.x >> 4;
+    pdl_wait();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int n = n0 + 4 * tn + a;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int k = k0 + 4 * tk + c;
+            acc[a][c] = (accumulate && n < N && k < D) ? dW_acc[(size_t)n * D + k] : 0.0f;
+        }
+    }
+    for (int b0 = 0; b0 < B; b0 += kDwBChunk) {
+        const int nb = min(kDwBChunk, B - b0);
+        for (int i = threadIdx.x; i < kDwBChunk * kDwTile; i += blockDim.x) {
+            const int b = i / kDwTile, j = i % kDwTile;
+            const int n = n0 + j, k = k0 + j;
+            es[b][j] = (b < nb && n < N) ? bf16f(bf16_bits(d_emb[(size_t)(b0 + b) * N + n])) : 0.0f;
+            us[b][j] = (b < nb && k < D) ? bf16f(u[(size_t)(b0 + b) * D + k]) : 0.0f;
+        }
+        __syncthreads();
+        for (int b = 0; b < nb; ++b) {
+            const float4 e4 = *reinterpret_cast<const float4 *>(&es[b][4 * tn]);
+            const float4 u4 = *reinterpret_cast<const float4 *>(&us[b][4 * tk]);
+            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+            const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][c] = __fmaf_rn(ev[a], uv[c], acc[a][c]);
+        }
+        __syncthreads();
+    }
+    pdl_trigger();
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int n = n0 + 4 * tn + a;
+        const int k = k0 + 4 * tk;
+        if (n < N && k < D) {  // D % 8 == 0, so the 4 columns are all in range
+            if (dW_acc) stg16f(dW_acc + (size_t)n * D + k, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
+            if (dW) {
+                uint2 p;
+                p.x = pack_bf16x2(acc[a][0], acc[a][1]);
+                p.y = pack_bf16x2(acc[a][2], acc[a][3]);
+                *reinterpret_cast<uint2 *>(dW + (size_t)n * D + k) = p;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256)
+proj_db_kernel(const float *__restrict__ d_emb, float *__restrict__ db_acc, uint16_t *__restrict__ db, int accumulate,
+               int B, int N) {
+    pdl_wait();
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n < N) {
+        float a = accumulate ? db_acc[n] : 0.0f;
+        for (int b = 0; b < B; ++b) a = __fadd_rn(a, bf16f(bf16_bits(d_emb[(size_t)b * N + n])));
+        if (db_acc) db_acc[n] = a;
+        if (db) db[n] = bf16_bits(a);
+    }
+    pdl_trigger();
+}
+
+// --------------------------------------------------------------------------
+// launchers
+// --------------------------------------------------------------------------
+template <int BC>
+static cudaError_t launch_proj_fwd_gemv(const uint16_t *W, const uint16_t *bias, const uint16_t *u, uint16_t *emb,
+                                        int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
+    const size_t smem = (size_t)BC * D * 2;
+    auto kern = proj_fwd_kernel<BC>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3((2 * D + 7) / 8), dim3(256), smem, stream, W, bias, u, emb, B, D);
+}
+
+cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
+                            uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
+    const long long n8 = (long long)B * D / 8;
+    cudaError_t err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
+    if (err != cudaSuccess) return err;
+    if (B == 1) return launch_proj_fwd_gemv<1>(W, bias, u, emb, B, D, stream, dev);
+    if (B == 2) return launch_proj_fwd_gemv<2>(W, bias, u, emb, B, D, stream, dev);
+    if (B <= 4) return launch_proj_fwd_gemv<4>(W, bias, u, emb, B, D, stream, dev);
+    return launch_proj_fwd_gemv<8>(W, bias, u, emb, B, D, stream, dev);
+}
+
+template <int BC, bool WITH_W>
+static cudaError_t launch_slab(const float *d_emb, const uint16_t *u, const uint16_t *W, float *dW_acc, float *db_acc,
+                               uint16_t *dW, uint16_t *db, int accumulate, float *ws, int B, int D,
+                               cudaStream_t stream, const DeviceInfo &dev) {
+    const size_t smem = sizeof(SlabSmem<BC>);
+    auto kern = proj_bwd_slab_kernel<BC, WITH_W>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
+    if (err != cudaSuccess) return err;
+    const int nslab = (2 * D + kSlabRows - 1) / kSlabRows;
+    const int nk = (D + kProjKChunk - 1) / kProjKChunk;
+    return launch_pdl(kern, dim3(nk, nslab), dim3(256), smem, stream, d_emb, u, W, dW_acc, db_acc, dW, db,
+                      accumulate, ws, B, D);
+}
+
+cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
+                            uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
+                            int accumulate, void *ws_v, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
+    float *ws = static_cast<float *>(ws_v);
+    const int N = 2 * D;
+    const int nslab = (N + kSlabRows - 1) / kSlabRows;
+    cudaError_t err;
+    if (B <= 4) {
+        // one pass over W: d_silu partials and (when asked) dW / db
+        if (B <= 1) err = launch_slab<1, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+        else if (B == 2) err = launch_slab<2, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+        else err = launch_slab<4, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+    } else {
+        err = launch_slab<4, false>(d_emb, u, W, nullptr, nullptr, nullptr, nullptr, 0, ws, B, D, stream, dev);
+        if (err == cudaSuccess && (dW_acc || dW))
+            err = launch_pdl(proj_dw_tiled_kernel, dim3((D + kDwTile - 1) / kDwTile, (N + kDwTile - 1) / kDwTile),
+                             dim3(256), 0, stream, d_emb, u, dW_acc, dW, accumulate, B, D);
+        if (err == cudaSuccess && (db_acc || db))
+            err = launch_pdl(proj_db_kernel, dim3((N + 255) / 256), dim3(256), 0, stream, d_emb, db_acc, db,
+                             accumulate, B, N);
+    }
+    if (err != cudaSuccess || B == 0) return err;
+    const long long BD = (long long)B * D;
+    return launch_pdl(proj_bwd_final_kernel, dim3((unsigned)((BD + 255) / 256)), dim3(256), 0, stream, ws, temb,
+                      d_temb, B, D, nslab);
+}
+
+}  // namespace adaln
