@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the AdaLN norm_out forward + backward on GB300.
+
+One step = the whole hot path on one batch of synthetic inputs already in
+HBM: adaln_proj_fwd, adaln_out_fwd, adaln_out_bwd, adaln_proj_bwd (bf16 dW,
+db) at B=2, S=4096, D=3072 with 1% outlier rows.  The headline is tokens/s;
+the JSON line also carries HBM GB/s from the algorithmic bytes, the roofline
+of the dominant call, an end-to-end number through host buffers, the CPU
+oracle's throughput and the SM clocks seen during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica (weak scaling; the
+path has no cross-sample exchange), the elapsed time is the max over ranks
+and rank 0 prints one JSON line.  --impl reference runs the CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AdaLN-out fwd+bwd tokens/s and HBM GB/s (% of 8 TB/s) at B=2,S=4096,D=3072"
+WORKLOAD = dict(B=2, S=4096, D=3072, seed=0, outlier_frac=0.01)
+NOMINAL_HBM_GBS = 8000.0
+FLUSH_BYTES = 512 << 20
+KERNELS_PER_STEP = 7  # silu, projection, out_fwd, bwd tile, tree fold, proj-bwd slab, d_temb
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; workspaces excluded)
+# ---------------------------------------------------------------------------
+
+def call_bytes(B, S, D):
+    """Bytes each C-ABI call must read and write once, by tensor sizes."""
+    N = 2 * D
+    rows = B * S
+    bf, f4 = 2, 4
+    return {
+        "adaln_proj_fwd": B * D * bf + N * D * bf + N * bf + B * N * bf + B * D * bf,
+        "adaln_out_fwd": rows * D * bf + B * N * bf + rows * D * bf + 2 * rows * f4,
+        "adaln_out_bwd": 2 * rows * D * bf + B * N * bf + 2 * rows * f4 + rows * D * bf + B * N * f4,
+        "adaln_proj_bwd": B * N * f4 + 2 * B * D * bf + N * D * bf + B * D * bf + N * D * bf + N * bf,
+    }
+
+
+def step_bytes(B, S, D):
+    return sum(call_bytes(B, S, D).values())
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host side; also exercised on CPU with gloo)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist_mod, device=None):
+    if dist_mod is not None:
+        if device is not None:
+            dist_mod.barrier(device_ids=[device.index])
+        else:
+            dist_mod.barrier()
+
+
+def max_over_ranks(value: float, dist_mod, device=None) -> float:
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the max time."""
+    return units_per_rank * world / seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[4:8]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (a bounded sample of the workload)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(oracle, inp, frac, emb_full=None):
+    """The oracle's chain on a fraction `frac` of the workload, so that every
+    stage does `frac` of its full work: the projection forward and backward on
+    the first frac*2D output rows, the LayerNorm forward and backward on the
+    first frac*S tokens of every sample (with the full emb).  frac = 1 is the
+    whole workload through the oracle's full entry points.  Returns seconds."""
+    B, S, D = inp["x"].shape
+    t0 = time.perf_counter()
+    if frac >= 1:
+        emb = oracle.proj_fwd(inp["temb"], inp["W"], inp["b"])
+        _, _, _ = oracle.out_fwd(inp["x"], emb)
+        _, d_emb = oracle.out_bwd(inp["dy"], inp["x"], emb)
+        oracle.proj_bwd(d_emb, inp["temb"], inp["W"])
+        return time.perf_counter() - t0
+    s = max(1, int(round(S * frac)))
+    n = max(1, int(round(2 * D * frac)))
+    oracle.proj_fwd_rows(inp["temb"], inp["W"], inp["b"], 0, n, emb=emb_full.copy())
+    x = np.ascontiguousarray(inp["x"][:, :s])
+    dy = np.ascontiguousarray(inp["dy"][:, :s])
+    oracle.out_fwd(x, emb_full)
+    _, d_emb = oracle.out_bwd(dy, x, emb_full)
+    oracle.proj_bwd_rows(d_emb, inp["temb"], inp["W"], 0, n)
+    return time.perf_counter() - t0
+
+
+def time_oracle(inp, budget_s=12.0, max_steps=50):
+    """Run the full oracle chain repeatedly for about budget_s seconds."""
+    import oracle
+    oracle.build()
+    B, S, _ = inp["x"].shape
+    times = []
+    t_start = time.perf_counter()
+    while not times or (time.perf_counter() - t_start < budget_s and len(times) < max_steps):
+        times.append(oracle_sample_step(oracle, inp, 1.0))
+    total = sum(times)
+    return {"value": B * S * len(times) / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} full steps of B={B}, S={S} (all tokens, all projection rows), single thread",
+            "seconds": total}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_mod = init_dist(world, "nccl")
+    build.build()
+    binding.load()
+
+    W_ = WORKLOAD
+    B, S, D = W_["B"], W_["S"], W_["D"]
+    N = 2 * D
+    host = synth.make_inputs(B, S, D, seed=W_["seed"] + rank, outlier_frac=W_["outlier_frac"])
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    x, dy, temb, W, b = (dev(host[k]) for k in ("x", "dy", "temb", "W", "b"))
+    emb = torch.empty((B, N), dtype=torch.bfloat16, device=device)
+    u = torch.empty((B, D), dtype=torch.bfloat16, device=device)
+    out = torch.empty((B, S, D), dtype=torch.bfloat16, device=device)
+    mean = torch.empty((B, S), dtype=torch.float32, device=device)
+    rstd = torch.empty((B, S), dtype=torch.float32, device=device)
+    dx = torch.empty_like(out)
+    d_emb = torch.empty((B, N), dtype=torch.float32, device=device)
+    d_temb = torch.empty((B, D), dtype=torch.bfloat16, device=device)
+    dW = torch.empty((N, D), dtype=torch.bfloat16, device=device)
+    db = torch.empty((N,), dtype=torch.bfloat16, device=device)
+    ws_bwd = torch.empty(binding.adaln_out_bwd_workspace_bytes(B, S, D), dtype=torch.uint8, device=device)
+    ws_proj = torch.empty(binding.adaln_proj_bwd_workspace_bytes(B, D), dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=stream)
+        binding.adaln_out_fwd(x, emb, out=out, mean=mean, rstd=rstd, stream=stream)
+        binding.adaln_out_bwd(dy, x, emb, mean, rstd, dx=dx, d_emb=d_emb, workspace=ws_bwd, stream=stream)
+        binding.adaln_proj_bwd(d_emb, temb, u, W, d_temb=d_temb, dW=dW, db=db, workspace=ws_proj, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+
+    # ---- timed region: K steps, per-step events, L2 flushed between steps ----
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(dist_mod, device)
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    barrier(dist_mod, device)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    my_time = sum(step_ms) / 1e3
+    t_max = max_over_ranks(my_time, dist_mod, device)
+    assert binding.device_error() == 0
+
+    # ---- per-call pass: events around each call (roofline of the dominant call) ----
+    K2 = min(K, 300)
+    names = ["adaln_proj_fwd", "adaln_out_fwd", "adaln_out_bwd", "adaln_proj_bwd"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K2)]
+    calls = [
+        lambda: binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=stream),
+        lambda: binding.adaln_out_fwd(x, emb, out=out, mean=mean, rstd=rstd, stream=stream),
+        lambda: binding.adaln_out_bwd(dy, x, emb, mean, rstd, dx=dx, d_emb=d_emb, workspace=ws_bwd, stream=stream),
+        lambda: binding.adaln_proj_bwd(d_emb, temb, u, W, d_temb=d_temb, dW=dW, db=db, workspace=ws_proj,
+                                       stream=stream),
+    ]
+    for i in range(K2):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    call_ms = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K2)) for j, n in enumerate(names)}
+
+    # ---- end to end: host buffers in, host buffers out, every step ----
+    K3 = min(K, 100)
+    pin = {k: torch.from_numpy(np.ascontiguousarray(host[k]).view(np.int16)).view(torch.bfloat16).pin_memory()
+           for k in ("x", "dy", "temb", "W", "b")}
+    outs_h = {"out": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+              "dx": torch.empty(dx.shape, dtype=dx.dtype).pin_memory(),
+              "emb": torch.empty(emb.shape, dtype=emb.dtype).pin_memory(),
+              "d_emb": torch.empty(d_emb.shape, dtype=d_emb.dtype).pin_memory(),
+              "d_temb": torch.empty(d_temb.shape, dtype=d_temb.dtype).pin_memory(),
+              "dW": torch.empty(dW.shape, dtype=dW.dtype).pin_memory(),
+              "db": torch.empty(db.shape, dtype=db.dtype).pin_memory()}
+    dev_out = {"out": out, "dx": dx, "emb": emb, "d_emb": d_emb, "d_temb": d_temb, "dW": dW, "db": db}
+    dev_in = {"x": x, "dy": dy, "temb": temb, "W": W, "b": b}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    for i in range(K3):
+        flush.zero_()
+        e0[i].record(stream)
+        for k, t in pin.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        step()
+        for k, t in outs_h.items():
+            t.copy_(dev_out[k], non_blocking=True)
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(c) for a, c in zip(e0, e1)) / 1e3
+    e2e_max = max_over_ranks(e2e_s, dist_mod, device)
+    assert binding.device_error() == 0
+
+    tokens = B * S
+    value = throughput(tokens * K, world, t_max)
+    sbytes = step_bytes(B, S, D)
+    gbs = sbytes * K / my_time / 1e9
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    cb = call_bytes(B, S, D)
+    dom = "adaln_out_bwd"
+    ach = cb[dom] / (call_ms[dom] / 1e3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": my_time / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "compute": "fp32 arithmetic on bf16 tensors",
+        "data": "synthetic (seeded; x, dy ~ N(0,1) with 81 outlier rows x50; W, b ~ N(0, 0.02^2))",
+        "config": {"workload": "AdaLN norm_out fwd+bwd, B=2 S=4096 D=3072, 1% outlier rows",
+                   "B": B, "S": S, "D": D, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (512 MiB write outside the timed events); inputs 138 MB > L2"},
+        "hbm_gbs": gbs,
+        "hbm_frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+        "hbm_frac_of_measured": gbs / peak,
+        "algorithmic_bytes_per_step": sbytes,
+        "calls_ms": call_ms,
+        "roofline": {"bound": "hbm", "kernel": dom + " (LN-backward tile kernel + tree fold)",
+                     "achieved": ach, "peak": peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                     "algorithmic_bytes": cb[dom]},
+        "step_roofline": {"achieved": gbs, "peak": peak, "frac": gbs / peak, "unit": "GB/s"},
+        "e2e": {"value": throughput(tokens * K3, world, e2e_max), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = time_oracle(host, budget_s=args.cpu_budget)
+    if dist_mod is not None:
+        dist_mod.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the same workload
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    from invariant_dit_adaln_gb300 import synth
+    oracle.build()
+    W_ = WORKLOAD
+    B, S, D = W_["B"], W_["S"], W_["D"]
+    inp = synth.make_inputs(B, S, D, seed=W_["seed"], outlier_frac=W_["outlier_frac"])
+    # size the sample so that warmup + steps take about args.ref_budget seconds
+    emb_full = oracle.proj_fwd(inp["temb"], inp["W"], inp["b"])
+    t_cal = oracle_sample_step(oracle, inp, 1.0 / 64, emb_full)
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1.0 / 1024, (1.0 / 64) * per_step / max(t_cal, 1e-6)))
+    frac = float(2.0 ** np.floor(np.log2(frac)))
+    for _ in range(args.warmup):
+        oracle_sample_step(oracle, inp, frac, emb_full)
+    times = [oracle_sample_step(oracle, inp, frac, emb_full) for _ in range(args.steps)]
+    total = sum(times)
+    tokens = B * S * frac * len(times)
+    value = tokens / total
+    sample = (f"each step: the oracle chain on {frac:g} of the workload (first {max(1, int(round(S * frac)))} "
+              f"tokens of each of B={B} samples, {max(1, int(round(2 * D * frac)))} of {2 * D} projection rows), "
+              f"single thread")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle; bf16 rounding points emulated)",
+        "data": "synthetic (seeded; same inputs as the GPU arm)",
+        "config": {"workload": "AdaLN norm_out fwd+bwd, B=2 S=4096 D=3072, 1% outlier rows",
+                   "B": B, "S": S, "D": D, "parallelism": "CPU, rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm's steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_gpu(args, world, rank, local)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -50,6 +50,8 @@ def _load():
             "oracle_silu_bf16": [P, P, Lg],
             "oracle_dsilu_f64": [P, P, Lg],
             "oracle_proj_fwd": [P, P, P, P, I, I],
+            "oracle_proj_fwd_rows": [P, P, P, P, I, I, I, I],
+            "oracle_proj_bwd_rows": [P, P, P, P, P, P, I, I, I, I],
             "oracle_proj_fwd_f64": [P, P, P, P, I, I],
             "oracle_out_fwd": [P, P, F, P, P, P, I, I, I],
             "oracle_out_fwd_f64": [P, P, P, Dd, P, I, I, I],
@@ -106,6 +108,17 @@ def proj_fwd(temb, W, b):
     assert W.shape == (2 * D, D) and b.shape == (2 * D,)
     emb = np.empty((B, 2 * D), dtype=np.uint16)
     _load().oracle_proj_fwd(_p(temb), _p(W), _p(b), _p(emb), B, D)
+    return emb
+
+
+def proj_fwd_rows(temb, W, b, n0, n1, emb=None):
+    """The projection for the output rows n0 <= n < n1 only (others of
+    ``emb`` are left as given)."""
+    temb, W, b = _c(temb, np.uint16), _c(W, np.uint16), _c(b, np.uint16)
+    B, D = temb.shape
+    assert 0 <= n0 <= n1 <= 2 * D
+    emb = np.zeros((B, 2 * D), dtype=np.uint16) if emb is None else _c(emb, np.uint16)
+    _load().oracle_proj_fwd_rows(_p(temb), _p(W), _p(b), _p(emb), B, D, n0, n1)
     return emb
 
 
@@ -198,6 +211,20 @@ def proj_bwd(d_emb, temb, W, want_dW=True):
     db = np.empty(2 * D, dtype=np.float64)
     _load().oracle_proj_bwd(_p(d_emb), _p(temb), _p(W), _p(d_temb), _p(dW), _p(db), B, D)
     return d_temb, dW, db
+
+
+def proj_bwd_rows(d_emb, temb, W, n0, n1, want_dW=True):
+    """The projection backward's sums over the output rows n0 <= n < n1:
+    (d_silu partial fp64 [B,D], dW fp64 [2D,D] (rows n0..n1 filled) or None,
+    db fp64 [2D] (rows n0..n1 filled))."""
+    d_emb, temb, W = _c(d_emb, np.float32), _c(temb, np.uint16), _c(W, np.uint16)
+    B, D = temb.shape
+    assert 0 <= n0 <= n1 <= 2 * D
+    d_silu = np.empty((B, D), dtype=np.float64)
+    dW = np.zeros((2 * D, D), dtype=np.float64) if want_dW else None
+    db = np.zeros(2 * D, dtype=np.float64)
+    _load().oracle_proj_bwd_rows(_p(d_emb), _p(temb), _p(W), _p(d_silu), _p(dW), _p(db), B, D, n0, n1)
+    return d_silu, dW, db
 
 
 def proj_bwd_f64(d_emb, temb, W):

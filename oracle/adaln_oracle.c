@@ -38,7 +38,9 @@
  *
  *  - LayerNorm variance is the biased one (divide by D), eps = fp32(1e-6) is
  *    added to the variance inside the square root.
- *  - SiLU output u is bf16(silu(t)), the nearest bf16 to the exact value.
+ *  - SiLU output u is the bf16 nearest to the fp64 value of t/(1+exp(-t))
+ *    (the correctly rounded SiLU for every |t| >= 2^-125; below that the fp64
+ *    value is t/2 and can sit on a bf16 tie).
  *  - The projection bias is added before the single bf16 rounding of emb.
  *  - onep = bf16(fp32(1 + scale)); m = fp32(fp32(xhat * onep) + shift), xhat
  *    being the fp32 rounding of the exact LayerNorm value; out = bf16(m).
@@ -131,12 +133,13 @@ void oracle_dsilu_f64(const double *t, double *out, long n)
 /* shared cores                                                              */
 /* ------------------------------------------------------------------------ */
 
-/* emb[b,n] = sum_k u[b,k] * W[n,k] + bias[n], compensated fp64 */
+/* emb[b,n] = sum_k u[b,k] * W[n,k] + bias[n], compensated fp64, for the
+ * output rows n0 <= n < n1 (emb keeps its row stride N)                    */
 static void proj_core(const double *u, const double *W, const double *bias,
-                      double *emb, int B, int K, int N)
+                      double *emb, int B, int K, int N, int n0, int n1)
 {
     for (int b = 0; b < B; ++b)
-        for (int n = 0; n < N; ++n) {
+        for (int n = n0; n < n1; ++n) {
             nsum acc = {0.0, 0.0};
             const double *w = W + (size_t)n * K;
             const double *ub = u + (size_t)b * K;
@@ -179,9 +182,10 @@ static void ln_bwd_row(const double *gh, const double *xhat, double rstd, int D,
 /* ------------------------------------------------------------------------ */
 
 /* emb = bf16( bf16(silu(temb)) @ W^T + b ); W is [2D, D] row-major,
- * emb [B, 2D] = [scale | shift].                                            */
-void oracle_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
-                     uint16_t *emb, int B, int D)
+ * emb [B, 2D] = [scale | shift].  Only the output rows n0 <= n < n1 are
+ * written (oracle_proj_fwd: all of them).                                   */
+void oracle_proj_fwd_rows(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
+                          uint16_t *emb, int B, int D, int n0, int n1)
 {
     int N = 2 * D;
     double *u = malloc(sizeof(double) * (size_t)B * D);
@@ -189,11 +193,18 @@ void oracle_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bi
     double *bb = malloc(sizeof(double) * (size_t)N);
     double *e = malloc(sizeof(double) * (size_t)B * N);
     for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f64(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
-    for (size_t i = 0; i < (size_t)N * D; ++i) w[i] = bf16_to_f64(W[i]);
-    for (int n = 0; n < N; ++n) bb[n] = bf16_to_f64(bias[n]);
-    proj_core(u, w, bb, e, B, D, N);
-    for (size_t i = 0; i < (size_t)B * N; ++i) emb[i] = bf16_from_f64(e[i]);
+    for (size_t i = (size_t)n0 * D; i < (size_t)n1 * D; ++i) w[i] = bf16_to_f64(W[i]);
+    for (int n = n0; n < n1; ++n) bb[n] = bf16_to_f64(bias[n]);
+    proj_core(u, w, bb, e, B, D, N, n0, n1);
+    for (int b = 0; b < B; ++b)
+        for (int n = n0; n < n1; ++n) emb[(size_t)b * N + n] = bf16_from_f64(e[(size_t)b * N + n]);
     free(u); free(w); free(bb); free(e);
+}
+
+void oracle_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
+                     uint16_t *emb, int B, int D)
+{
+    oracle_proj_fwd_rows(temb, W, bias, emb, B, D, 0, 2 * D);
 }
 
 /* the same map without any rounding */
@@ -203,7 +214,7 @@ void oracle_proj_fwd_f64(const double *temb, const double *W, const double *bias
     int N = 2 * D;
     double *u = malloc(sizeof(double) * (size_t)B * D);
     for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = silu64(temb[i]);
-    proj_core(u, W, bias, emb, B, D, N);
+    proj_core(u, W, bias, emb, B, D, N, 0, N);
     free(u);
 }
 
@@ -438,45 +449,67 @@ void oracle_bwd_products_f32(const uint16_t *dy, const uint16_t *x, const float 
 /* projection backward                                                       */
 /* ------------------------------------------------------------------------ */
 
+/* The sums of the projection backward over the output rows n0 <= n < n1:
+ * d_silu[b,k] += sum_n e[b,n] W[n,k] (Neumaier accumulators acc[b*D+k]),
+ * dW[n,k] = sum_b e[b,n] u[b,k], db[n] = sum_b e[b,n] (fp64, compensated).  */
+static void proj_bwd_rows_core(const double *e, const double *u, const uint16_t *W, nsum *acc,
+                               double *dW, double *db, int B, int D, int n0, int n1)
+{
+    int N = 2 * D;
+    for (int b = 0; b < B; ++b)
+        for (int n = n0; n < n1; ++n) {
+            double en = e[(size_t)b * N + n];
+            const uint16_t *w = W + (size_t)n * D;
+            for (int k = 0; k < D; ++k) nsum_add(&acc[(size_t)b * D + k], en * bf16_to_f64(w[k]));
+        }
+    for (int n = n0; n < n1; ++n) {
+        if (dW)
+            for (int k = 0; k < D; ++k) {
+                nsum a = {0.0, 0.0};
+                for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n] * u[(size_t)b * D + k]);
+                dW[(size_t)n * D + k] = nsum_val(&a);
+            }
+        if (db) {
+            nsum a = {0.0, 0.0};
+            for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n]);
+            db[n] = nsum_val(&a);
+        }
+    }
+}
+
 /* e = bf16(d_emb); u = bf16(silu(temb));
  * d_temb[b,k] = bf16( (sum_n e[b,n] W[n,k]) * silu'(temb[b,k]) );
- * dW[n,k] = sum_b e[b,n] u[b,k];  db[n] = sum_b e[b,n]   (fp64, compensated) */
-void oracle_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *W,
-                     uint16_t *d_temb, double *dW, double *db, int B, int D)
+ * dW[n,k] = sum_b e[b,n] u[b,k];  db[n] = sum_b e[b,n]   (fp64, compensated).
+ * With rows n0 <= n < n1 only (oracle_proj_bwd_rows), d_temb is replaced by
+ * the fp64 partial d_silu over those rows, and dW/db cover those rows.     */
+static void proj_bwd_impl(const float *d_emb, const uint16_t *temb, const uint16_t *W,
+                          uint16_t *d_temb, double *d_silu, double *dW, double *db,
+                          int B, int D, int n0, int n1)
 {
     int N = 2 * D;
     double *e = malloc(sizeof(double) * (size_t)B * N);
     double *u = malloc(sizeof(double) * (size_t)B * D);
-    nsum *acc = malloc(sizeof(nsum) * (size_t)D);
+    nsum *acc = calloc((size_t)B * D, sizeof(nsum));
     for (size_t i = 0; i < (size_t)B * N; ++i) e[i] = bf16_to_f64(bf16_from_f32(d_emb[i]));
     for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f64(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
-    for (int b = 0; b < B; ++b) {
-        for (int k = 0; k < D; ++k) acc[k].s = acc[k].c = 0.0;
-        for (int n = 0; n < N; ++n) {
-            double en = e[(size_t)b * N + n];
-            const uint16_t *w = W + (size_t)n * D;
-            for (int k = 0; k < D; ++k) nsum_add(&acc[k], en * bf16_to_f64(w[k]));
-        }
-        for (int k = 0; k < D; ++k) {
-            double t = bf16_to_f64(temb[(size_t)b * D + k]);
-            d_temb[(size_t)b * D + k] = bf16_from_f64(nsum_val(&acc[k]) * dsilu64(t));
-        }
+    proj_bwd_rows_core(e, u, W, acc, dW, db, B, D, n0, n1);
+    for (size_t i = 0; i < (size_t)B * D; ++i) {
+        if (d_temb) d_temb[i] = bf16_from_f64(nsum_val(&acc[i]) * dsilu64(bf16_to_f64(temb[i])));
+        if (d_silu) d_silu[i] = nsum_val(&acc[i]);
     }
-    if (dW || db)
-        for (int n = 0; n < N; ++n) {
-            if (dW)
-                for (int k = 0; k < D; ++k) {
-                    nsum a = {0.0, 0.0};
-                    for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n] * u[(size_t)b * D + k]);
-                    dW[(size_t)n * D + k] = nsum_val(&a);
-                }
-            if (db) {
-                nsum a = {0.0, 0.0};
-                for (int b = 0; b < B; ++b) nsum_add(&a, e[(size_t)b * N + n]);
-                db[n] = nsum_val(&a);
-            }
-        }
     free(e); free(u); free(acc);
+}
+
+void oracle_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *W,
+                     uint16_t *d_temb, double *dW, double *db, int B, int D)
+{
+    proj_bwd_impl(d_emb, temb, W, d_temb, NULL, dW, db, B, D, 0, 2 * D);
+}
+
+void oracle_proj_bwd_rows(const float *d_emb, const uint16_t *temb, const uint16_t *W,
+                          double *d_silu, double *dW, double *db, int B, int D, int n0, int n1)
+{
+    proj_bwd_impl(d_emb, temb, W, NULL, d_silu, dW, db, B, D, n0, n1);
 }
 
 /* exact gradients of oracle_proj_fwd_f64 for upstream gradient d_emb */

@@ -235,7 +235,7 @@ def test_proj_bwd_accumulate_over_calls(B, D, split):
     assert_bitwise(host_f32(cb), one[1], "chunked db")
     # appending zero samples changes nothing
     z = torch.zeros((3, 2 * D), device="cuda")
-    binding.adaln_proj_bwd(z, temb[:3], u[:3], W, dW_acc=cW, db_acc=cb, accumulate=True)
+    binding.adaln_proj_bwd(z, temb[:1].repeat(3, 1), u[:1].repeat(3, 1), W, dW_acc=cW, db_acc=cb, accumulate=True)
     assert_bitwise(host_f32(cW), one[0], "zero padding")
 
 
