@@ -172,6 +172,36 @@ adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adal
                            const float *mean, const float *rstd, adaln_bf16 *dx, float *d_emb,
                            void *workspace, size_t workspace_bytes, int B, int S, int D, void *stream);
 
+/*
+ * adaln_out_bwd_noalloc — adaln_out_bwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this call; it exists for
+ * code that runs where allocation is not allowed: a plugin inside an engine
+ * that owns all device memory and forbids allocations in its execute hook, a
+ * real-time loop that must not take the allocator's locks or risk its
+ * implicit synchronisation, or a caller with a memory budget fixed at
+ * start-up.
+ *
+ * Same arguments, checks, kernels and results (bit for bit) as
+ * adaln_out_bwd, without the workspace: the token-tree partials live in a
+ * 24 MiB array inside the library, held on every GPU that loads the library
+ * until the process exits.  The call allocates nothing.
+ *
+ *   Limit: adaln_out_bwd_workspace_bytes(B, S, D) <= 24 MiB, i.e.
+ *   B * ceil(S/32) * 2D * 8 bytes <= 25165824 (at D = 3072: B * ceil(S/32)
+ *   <= 512, e.g. B = 2 with S <= 8192).  Larger sizes return ADALN_ERR_SHAPE
+ *   before anything is launched.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array: two calls whose kernels overlap on
+ * the GPU (different streams, no ordering between them) race on it and give
+ * wrong results.  Nothing in the array needs to start at zero: every partial
+ * the tree reads is written earlier in the same call.
+ */
+adaln_status adaln_out_bwd_noalloc(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb,
+                                   const float *mean, const float *rstd, adaln_bf16 *dx, float *d_emb,
+                                   int B, int S, int D, void *stream);
+
 /* Workspace bytes token_sum_tree needs: 2 * B * ceil(S/32) * H fp32 values,
  * rounded up to 256 bytes.  0 if B*S == 0. */
 size_t token_sum_tree_workspace_bytes(int B, int S, int H);

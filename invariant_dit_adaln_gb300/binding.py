@@ -31,6 +31,7 @@ _SIGNATURES = {
     "adaln_out_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P]),
     "adaln_out_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "adaln_out_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _P]),
+    "adaln_out_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "token_sum_tree_workspace_bytes": (_SZ, [_I, _I, _I]),
     "token_sum_tree": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P]),
     "adaln_proj_bwd_workspace_bytes": (_SZ, [_I, _I]),
@@ -194,6 +195,25 @@ def adaln_out_bwd(dy, x, emb, mean, rstd, dx=None, d_emb=None, workspace=None, s
     ws, nws = _workspace(workspace, L.adaln_out_bwd_workspace_bytes(B, S, D), x.device)
     _check("adaln_out_bwd", L.adaln_out_bwd(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd), _ptr(dx),
                                             _ptr(d_emb), _ptr(ws), nws, B, S, D, _stream(stream)))
+    return dx, d_emb
+
+
+def adaln_out_bwd_noalloc(dy, x, emb, mean, rstd, dx=None, d_emb=None, stream=None):
+    """adaln_out_bwd without a workspace, for callers that cannot allocate
+    device memory at this point: the tree partials use a 24 MiB array inside
+    the library.  dx and d_emb must be passed in for a call that allocates
+    nothing (otherwise they are allocated here).  Returns (dx, d_emb)."""
+    L = load()
+    B, S, D = x.shape
+    dy = _input(dy, torch.bfloat16, (B, S, D), "dy")
+    x = _input(x, torch.bfloat16, (B, S, D), "x")
+    emb = _input(emb, torch.bfloat16, (B, 2 * D), "emb")
+    mean = _input(mean, torch.float32, (B, S), "mean")
+    rstd = _input(rstd, torch.float32, (B, S), "rstd")
+    dx = _output(dx, torch.bfloat16, (B, S, D), "dx", x.device)
+    d_emb = _output(d_emb, torch.float32, (B, 2 * D), "d_emb", x.device)
+    _check("adaln_out_bwd_noalloc", L.adaln_out_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd),
+                                                            _ptr(dx), _ptr(d_emb), B, S, D, _stream(stream)))
     return dx, d_emb
 
 

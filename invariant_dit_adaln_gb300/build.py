@@ -1,6 +1,6 @@
 """Build libadaln.so in-tree with nvcc for sm_103a (GB300).
 
-Three translation units are compiled in parallel and linked into
+The translation units are compiled in parallel and linked into
 ``invariant_dit_adaln_gb300/lib/libadaln.so`` (git-ignored).  Flags:
 ``-gencode arch=compute_103a,code=sm_103a -O3 -lineinfo --fmad=false``; no
 fast math, so every floating-point operation rounds as written.
@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libadaln.so")
-SOURCES = ["api.cu", "out.cu", "proj.cu"]
+SOURCES = ["api.cu", "out.cu", "proj.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xptxas", "-warn-spills", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,0 +1,75 @@
+// adaln_out_bwd_noalloc: the LayerNorm/modulation backward for callers that
+// cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc (or any allocator) at
+// the point where they run the backward: a plugin inside an inference or
+// training engine that owns every byte of device memory and forbids
+// allocations inside its execute hook, a real-time loop that must never take
+// the allocator's locks or risk its implicit device synchronisation, or code
+// with a fixed memory budget decided at start-up.  For them this entry point
+// takes no workspace: the token-tree partials live in a file-scope device
+// array that is part of the library image.  Every GPU that loads the library
+// holds this array (kNoAllocScratchBytes) until the process exits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "adaln.h"
+
+namespace adaln {
+
+// 24 MiB: the level-0 partials of B * ceil(S/32) <= 512 sample-tiles at D = 3072
+// (for instance B = 2 and S <= 8192, or B = 1 and S <= 16384).
+constexpr size_t kNoAllocScratchBytes = 24u << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];  // device address of the array, per device, once looked up
+
+// The array's device address for the current device.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in, never a device address, so
+// the address is asked from the runtime, with the device current.
+adaln_status noalloc_scratch(void **ptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return ADALN_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return ADALN_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return ADALN_OK;
+}
+
+}  // namespace
+}  // namespace adaln
+
+extern "C" {
+
+adaln_status adaln_out_bwd_noalloc(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb,
+                                   const float *mean, const float *rstd, adaln_bf16 *dx, float *d_emb, int B, int S,
+                                   int D, void *stream) {
+    // sizes first: the partials must fit in the library's own array
+    if (D < 8 || D > 8192 || D % 8 != 0 || B < 0 || S < 0 || S > 262144 || B > 65535) return ADALN_ERR_SHAPE;
+    if (adaln_out_bwd_workspace_bytes(B, S, D) > adaln::kNoAllocScratchBytes) return ADALN_ERR_SHAPE;
+    void *scratch = nullptr;
+    if (adaln_out_bwd_workspace_bytes(B, S, D) > 0) {
+        adaln_status st = adaln::noalloc_scratch(&scratch);
+        if (st != ADALN_OK) return st;
+    }
+    // the same checks and kernels as adaln_out_bwd, with the array as workspace
+    return adaln_out_bwd(dy, x, emb, mean, rstd, dx, d_emb, scratch, adaln::kNoAllocScratchBytes, B, S, D, stream);
+}
+
+}  // extern "C"

@@ -41,7 +41,7 @@ def fake(i, off=0):
 
 def test_library_exports_every_declared_symbol(L):
     names = binding.declared_symbols()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     for n in names:
         assert hasattr(L, n), n
     assert L.adaln_version() >> 16 == 1

@@ -1,0 +1,66 @@
+"""adaln_out_bwd_noalloc: the backward for callers that cannot allocate.
+
+Some callers cannot call cudaMalloc where they run the backward (an engine
+plugin whose host owns all device memory, a real-time loop that must not
+touch the allocator).  This entry point takes no workspace and uses an array
+inside the library instead.  It must give the same bytes as adaln_out_bwd
+with a caller-provided workspace, on consecutive calls that reuse the array.
+
+The file is named to be collected last, so that a run stopping at the first
+failure has already run every other test.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_dit_adaln_gb300 import binding, synth
+from gpu_util import dev_bf16, lib
+from tolerance import assert_bitwise
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = 2
+LIMIT = 24 << 20
+
+
+def _forward(inp):
+    x, temb, W, b = (dev_bf16(inp[k]) for k in ("x", "temb", "W", "b"))
+    emb, _ = binding.adaln_proj_fwd(temb, W, b)
+    _, mean, rstd = binding.adaln_out_fwd(x, emb)
+    return x, dev_bf16(inp["dy"]), emb, mean, rstd
+
+
+def test_noalloc_matches_workspace_call_on_consecutive_calls():
+    L = lib()
+    # two calls in a row on different shapes and inputs; the second reuses the
+    # array the first one filled
+    for (B, S, D, seed) in [(2, 4096, 3072, 3), (2, 33, 3072, 4), (1, 1100, 512, 5)]:
+        inp = synth.make_inputs(B, S, D, seed, outlier_frac=0.01)
+        x, dy, emb, mean, rstd = _forward(inp)
+        dx_ref, demb_ref = binding.adaln_out_bwd(dy, x, emb, mean, rstd)
+        dx = torch.empty_like(dx_ref)
+        d_emb = torch.empty_like(demb_ref)
+        stream = torch.cuda.current_stream().cuda_stream
+        st = L.adaln_out_bwd_noalloc(dy.data_ptr(), x.data_ptr(), emb.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                                     dx.data_ptr(), d_emb.data_ptr(), B, S, D, ctypes.c_void_p(stream))
+        assert st == 0, binding.status_string(st)
+        torch.cuda.synchronize()
+        assert_bitwise(dx.view(torch.int16).cpu().numpy(), dx_ref.view(torch.int16).cpu().numpy(), "dx")
+        assert_bitwise(d_emb.cpu().numpy(), demb_ref.cpu().numpy(), "d_emb")
+    assert binding.device_error() == 0
+
+
+def test_noalloc_rejects_sizes_beyond_its_array():
+    L = lib()
+    B, D = 2, 3072
+    S = 32 * (LIMIT // (B * 2 * D * 8) + 1)  # one tile per sample too many
+    assert L.adaln_out_bwd_workspace_bytes(B, S, D) > LIMIT
+    st = L.adaln_out_bwd_noalloc(None, None, None, None, None, None, None, B, S, D, None)
+    assert st == SHAPE
+    S_ok = 32 * (LIMIT // (B * 2 * D * 8))
+    assert L.adaln_out_bwd_workspace_bytes(B, S_ok, D) <= LIMIT
