@@ -100,6 +100,11 @@ int adaln_version(void);
  *
  * The k-order of every dot product is fixed by D alone, so emb[b,:] does not
  * depend on B or on b.  B == 0 launches nothing.
+ *
+ * The first call with B > 0 on a device also fills a 128 KB SiLU lookup table
+ * in the library's device memory (a kernel on `stream`) and synchronizes
+ * `stream` once; make that first call outside stream capture.  Later calls
+ * neither synchronize nor touch the table's contents.
  */
 adaln_status adaln_proj_fwd(const adaln_bf16 *temb, const adaln_bf16 *W, const adaln_bf16 *bias,
                             adaln_bf16 *emb, adaln_bf16 *u, int B, int D, void *stream);
@@ -222,7 +227,7 @@ adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H,
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /* Workspace bytes adaln_proj_bwd needs: the per-slab d_silu partials,
- * ceil(2D/384) * B * D fp32 values, rounded up to 256 bytes. */
+ * ceil(2D/256) * B * D fp32 values, rounded up to 256 bytes. */
 size_t adaln_proj_bwd_workspace_bytes(int B, int D);
 
 /*

@@ -19,7 +19,7 @@ constexpr int kMaxD = 8192;
 constexpr int kMaxS = 262144;           // 32^3 * 8 tokens: at most 256 level-1 nodes
 constexpr int kTile = 32;               // the token tree's fan-out
 constexpr int kMaxLevel1 = kMaxS / (kTile * kTile);  // 256
-constexpr int kProjSlabRows = 384;      // rows of W per d_silu partial (fixed by D only)
+constexpr int kProjSlabRows = 256;      // rows of W per d_silu partial (fixed by D only)
 constexpr int kProjKChunk = 256;        // columns of W per projection-backward CTA
 
 // Error word (device side) set by a wait that ran out of time.
@@ -27,6 +27,7 @@ enum DeviceError : unsigned {
     kErrNone = 0,
     kErrOutFwdWait = 0x101,
     kErrOutBwdWait = 0x201,
+    kErrProjWait = 0x301,
 };
 
 // --------------------------------------------------------------------------
@@ -60,6 +61,26 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     v.w = pack_bf16x2(f[6], f[7]);
     return v;
 }
+
+// a packed bf16x2 word as (lo, hi) floats: exact
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// --------------------------------------------------------------------------
+// packed fp32x2 arithmetic (one instruction for two lanes of work on sm_103a),
+// each result rounded to nearest even, like the scalar __f*_rn forms.
+//
+// Caution: the compiler may merge a packed multiply into a packed add that
+// consumes it, giving one rounding where the source asks for two.  Where a
+// product must be rounded before it is added (the operator's x_hat * (1 +
+// scale) and the token products g * x_hat), the product is taken with the
+// scalar __fmul_rn, which --fmad=false keeps separate.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2splat(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+// a - b: b * (-1) is exact, so the fused form rounds once, like a subtraction
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
 
 // --------------------------------------------------------------------------
 // SiLU rounded to bf16: the nearest bf16 to the fp64 value of t/(1+exp(-t)).
@@ -98,6 +119,26 @@ __device__ __forceinline__ void neumaier(float &s, float &c, float v) {
     s = t;
 }
 
+// The same step without a branch (Knuth's TwoSum): t = s + v and the exact
+// error e of that add, so that s + v = t + e; then c += e.  Neumaier's branch
+// also computes the exact error of t (the operand of larger magnitude minus t
+// is exact, and adding the other operand to it is exact too), so both give
+// the same t and the same c, bit for bit, whenever t is finite.
+__device__ __forceinline__ void twosum(float &s, float &c, float v) {
+    const float t = __fadd_rn(s, v);
+    const float bp = __fsub_rn(t, s);
+    const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(v, bp));
+    c = __fadd_rn(c, e);
+    s = t;
+}
+__device__ __forceinline__ void twosum2(float2 &s, float2 &c, float2 v) {
+    const float2 t = f2add(s, v);
+    const float2 bp = f2sub(t, s);
+    const float2 e = f2add(f2sub(s, f2sub(t, bp)), f2sub(v, bp));
+    c = f2add(c, e);
+    s = t;
+}
+
 // --------------------------------------------------------------------------
 // warp reductions with a fixed butterfly; every lane ends with the same bits
 // (each pairwise add is commutative, so partners compute identical values).
@@ -105,6 +146,16 @@ __device__ __forceinline__ void neumaier(float &s, float &c, float v) {
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    return v;
+}
+
+// two sums at once (each with the butterfly of warp_sum)
+__device__ __forceinline__ float2 warp_sum2(float2 v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float2 o = make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.x, off), __shfl_xor_sync(0xFFFFFFFFu, v.y, off));
+        v = f2add(v, o);
+    }
     return v;
 }
 
@@ -163,6 +214,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Ask the memory system to bring [src, src + bytes) into L2 (no completion
+// to wait for).  L2 is the point of coherence, so this is safe even while the
+// preceding kernel may still write the range: later reads see its writes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // named barrier over `count` threads (a multiple of 32)

@@ -25,39 +25,56 @@ __device__ __forceinline__ void report_error(unsigned code) { atomicCAS(&g_err, 
 // Forward: one warp-group (128 threads) per token row, persistent.
 //
 // A CTA holds kWG warp-groups; each owns a contiguous range of rows and a ring
-// of K row buffers in shared memory, filled by 1-D bulk copies (the TMA
-// engine) that one thread issues K rows ahead.  Thread t of a warp-group owns
-// the 16-byte vectors v = t + 128 j (8 columns each) of every row, so its
-// modulation parameters stay in registers while the sample index is unchanged.
-// The reduction order over d: per thread in (j, element) order, a fixed xor
-// butterfly within the warp, then the four warps in ascending order.  It
-// depends on D only.
+// of kFwdStages row buffers in shared memory, filled by 1-D bulk copies (the
+// TMA engine).  Rows are taken in blocks of kFwdBlock: the row sums of the
+// block, one barrier, the means; the sums of squared deviations, one barrier,
+// the rstd values; then the outputs, recomputed from the staged rows, and a
+// barrier that frees the block's stages for refilling.  Thread t of a
+// warp-group owns the 16-byte vectors v = t + 128 j (8 columns each), so its
+// modulation parameters stay in registers while the sample is unchanged.  The
+// reduction order over d: per thread in (j, column pair) order, the two halves
+// of the pairs, a fixed xor butterfly within the warp, then the four warps in
+// ascending order.  It depends on D only.
 // ==========================================================================
-constexpr int kWG = 2;            // warp-groups per CTA
-constexpr int kFwdStages = 4;     // rows in flight per warp-group
+constexpr int kWG = 2;          // warp-groups per CTA
+constexpr int kFwdBlock = 4;    // most rows per block (a block of BLK rows, NST = 2 BLK stages:
+                                // two blocks in flight per warp-group)
 
-template <int VPT>
 struct FwdSmem {
-    // per warp-group: [slot 0/1][sum, sq][warp 0..3]
-    float red[kWG][2][2][4];
-    uint64_t full[kWG][kFwdStages];
+    float red[kWG][2][kFwdBlock][4];  // [warp-group][sum, squares][row of block][warp]
+    float mu[kWG][kFwdBlock], rs[kWG][kFwdBlock];
+    uint64_t full[kWG][2 * kFwdBlock];
 };
 
-template <int VPT>
-__global__ void __launch_bounds__(kWG * 128)
+// barrier of one warp-group, and a vote: is `flag` set in any of its threads?
+__device__ __forceinline__ bool wg_barrier_or(int id, bool flag) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((unsigned)flag), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+template <int VPT, int BLK, int NST, int MINB>
+__global__ void __launch_bounds__(kWG * 128, MINB)
 out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
                float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, long long R) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    FwdSmem<VPT> &sm = *reinterpret_cast<FwdSmem<VPT> *>(smem_raw);
+    FwdSmem &sm = *reinterpret_cast<FwdSmem *>(smem_raw);
     const int row_bytes = D * 2;
-    unsigned char *stages = smem_raw + ((sizeof(FwdSmem<VPT>) + 127) / 128) * 128;
+    unsigned char *stages = smem_raw + ((sizeof(FwdSmem) + 127) / 128) * 128;
 
     const int wg = threadIdx.x >> 7;
     const int t = threadIdx.x & 127;
     const int warp = t >> 5;
     const int lane = t & 31;
     const int V = D >> 3;
-    unsigned char *my_stages = stages + (size_t)wg * kFwdStages * row_bytes;
+    unsigned char *my_stages = stages + (size_t)wg * NST * row_bytes;
 
     const long long G = (long long)gridDim.x * kWG;
     const long long g = (long long)blockIdx.x * kWG + wg;
@@ -66,153 +83,362 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
     const int nrows = (int)(r_end - r_begin);
 
     if (t == 0) {
-        for (int s = 0; s < kFwdStages; ++s) mbar_init(&sm.full[wg][s], 1);
+        for (int s = 0; s < NST; ++s) mbar_init(&sm.full[wg][s], 1);
         fence_barrier_init();
+        // warm L2 with the first rows while the preceding kernel finishes
+        for (int i = 0; i < NST && i < nrows; ++i) bulk_prefetch_l2(x + (size_t)(r_begin + i) * D, row_bytes);
     }
     __syncthreads();
-    pdl_wait();  // inputs may come from the preceding kernel
+    pdl_wait();  // inputs may come from the preceding kernel: read them only now
+    pdl_trigger();
 
-    if (t == 0) {
-        for (int i = 0; i < kFwdStages && i < nrows; ++i) {
+    if (t == 0)
+        for (int i = 0; i < NST && i < nrows; ++i) {
             mbar_arrive_expect_tx(&sm.full[wg][i], row_bytes);
             bulk_g2s(my_stages + (size_t)i * row_bytes, x + (size_t)(r_begin + i) * D, row_bytes, &sm.full[wg][i]);
         }
-    }
 
-    uint32_t onep[VPT][4], shift[VPT][4];  // packed bf16x2 parameters of the current sample
+    float2 onep[VPT][4], shift[VPT][4];  // modulation parameters of the current sample, by column pair
     long long cur_b = -1;
-    const float invD_num = (float)D;
+    const float Df = (float)D;
 
-    for (int i = 0; i < nrows; ++i) {
-        const long long r = r_begin + i;
-        const long long b = r / S;
-        if (b != cur_b) {
-            cur_b = b;
-            const uint16_t *e = emb + (size_t)b * 2 * D;
+    for (int r0 = 0; r0 < nrows; r0 += BLK) {
+        const int nb = min(BLK, nrows - r0);
+        // ---- row sums ----
+        bool ok = true;
+        #pragma unroll
+        for (int jr = 0; jr < BLK; ++jr) if (jr < nb) {
+            const int i = r0 + jr;
+            const int st = i % NST;
+            ok = mbar_wait_bounded(&sm.full[wg][st], (uint32_t)(i / NST) & 1u) && ok;
+            const unsigned char *row = my_stages + (size_t)st * row_bytes;
+            float2 s1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int v = t + 128 * j;
+                if (v < V && ok) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + (size_t)v * 16);
+                    s1 = f2add(s1, bf16x2_to_f2(w.x));
+                    s1 = f2add(s1, bf16x2_to_f2(w.y));
+                    s1 = f2add(s1, bf16x2_to_f2(w.z));
+                    s1 = f2add(s1, bf16x2_to_f2(w.w));
+                }
+            }
+            const float s1f = warp_sum(__fadd_rn(s1.x, s1.y));
+            if (lane == 0) sm.red[wg][0][jr][warp] = s1f;
+        }
+        if (wg_barrier_or(1 + wg, !ok)) {
+            if (t == 0) {
+                report_error(kErrOutFwdWait);
+                // let the copies this warp-group issued finish before leaving
+                const int issued = min(nrows, r0 + NST);
+                for (int k = r0; k < issued; ++k)
+                    mbar_wait_bounded(&sm.full[wg][k % NST], (uint32_t)(k / NST) & 1u, 10000000ull);
+            }
+            return;
+        }
+        if (t < nb) {
+            float tot = sm.red[wg][0][t][0];
+            tot = __fadd_rn(tot, sm.red[wg][0][t][1]);
+            tot = __fadd_rn(tot, sm.red[wg][0][t][2]);
+            tot = __fadd_rn(tot, sm.red[wg][0][t][3]);
+            sm.mu[wg][t] = __fdiv_rn(tot, Df);
+        }
+        named_bar(1 + wg, 128);
+        // ---- sums of squared deviations ----
+        #pragma unroll
+        for (int jr = 0; jr < BLK; ++jr) if (jr < nb) {
+            const unsigned char *row = my_stages + (size_t)((r0 + jr) % NST) * row_bytes;
+            const float2 mu2 = f2splat(sm.mu[wg][jr]);
+            float2 s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int v = t + 128 * j;
                 if (v < V) {
-                    uint4 sc = ldg16(e + (size_t)v * 8);
-                    uint4 sh = ldg16(e + D + (size_t)v * 8);
-                    float f[8];
-                    unpack8(sc, f);
-                    float o[8];
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + (size_t)v * 16);
+                    const uint32_t wa[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) o[k] = __fadd_rn(1.0f, f[k]);
-                    uint4 op = pack8(o);  // onep = bf16(fp32(1 + scale))
-                    onep[j][0] = op.x; onep[j][1] = op.y; onep[j][2] = op.z; onep[j][3] = op.w;
-                    shift[j][0] = sh.x; shift[j][1] = sh.y; shift[j][2] = sh.z; shift[j][3] = sh.w;
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 c = f2sub(bf16x2_to_f2(wa[q]), mu2);
+                        s2 = f2fma(c, c, s2);
+                    }
                 }
             }
+            const float s2f = warp_sum(__fadd_rn(s2.x, s2.y));
+            if (lane == 0) sm.red[wg][1][jr][warp] = s2f;
         }
-        const int st = i % kFwdStages;
-        const uint32_t parity = (uint32_t)(i / kFwdStages) & 1u;
-        const bool ok = mbar_wait_bounded(&sm.full[wg][st], parity);
-
-        float xv[VPT][8];
-        float s1 = 0.0f;
-        const unsigned char *row = my_stages + (size_t)st * row_bytes;
+        named_bar(1 + wg, 128);
+        if (t < nb) {
+            float tq = sm.red[wg][1][t][0];
+            tq = __fadd_rn(tq, sm.red[wg][1][t][1]);
+            tq = __fadd_rn(tq, sm.red[wg][1][t][2]);
+            tq = __fadd_rn(tq, sm.red[wg][1][t][3]);
+            sm.rs[wg][t] = __frsqrt_rn(__fadd_rn(__fdiv_rn(tq, Df), eps));
+        }
+        named_bar(1 + wg, 128);
+        // ---- outputs ----
+        #pragma unroll
+        for (int jr = 0; jr < BLK; ++jr) if (jr < nb) {
+            const int i = r0 + jr;
+            const long long r = r_begin + i;
+            const long long b = r / S;
+            if (b != cur_b) {
+                cur_b = b;
+                const uint16_t *e = emb + (size_t)b * 2 * D;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = t + 128 * j;
-            if (v < V && ok) {
-                uint4 w = *reinterpret_cast<const uint4 *>(row + (size_t)v * 16);
-                unpack8(w, xv[j]);
-            } else {
+                for (int j = 0; j < VPT; ++j) {
+                    const int v = t + 128 * j;
+                    if (v < V) {
+                        const uint4 sc = ldg16(e + (size_t)v * 8);
+                        const uint4 sh = ldg16(e + D + (size_t)v * 8);
+                        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+                        const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) xv[j][k] = 0.0f;
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = bf16x2_to_f2(scw[q]);
+                            // onep = bf16(fp32(1 + scale))
+                            onep[j][q] = make_float2(bf16f(bf16_bits(__fadd_rn(1.0f, f.x))),
+                                                     bf16f(bf16_bits(__fadd_rn(1.0f, f.y))));
+                            shift[j][q] = bf16x2_to_f2(shw[q]);
+                        }
+                    }
+                }
             }
+            const unsigned char *row = my_stages + (size_t)(i % NST) * row_bytes;
+            const float mu = sm.mu[wg][jr], rs = sm.rs[wg][jr];
+            const float2 mu2 = f2splat(mu), rs2 = f2splat(rs);
+            uint16_t *orow = out + (size_t)r * D;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s1 = __fadd_rn(s1, xv[j][k]);
-        }
-        s1 = warp_sum(s1);
-        const int slot = i & 1;
-        if (lane == 0) sm.red[wg][slot][0][warp] = s1;
-        // barrier of the warp-group, and a vote: did any thread time out?
-        int bad;
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\t"
-            "setp.ne.u32 p, %1, 0;\n\t"
-            "bar.red.or.pred q, %2, 128, p;\n\t"
-            "selp.u32 %0, 1, 0, q;\n\t}"
-            : "=r"(bad)
-            : "r"((unsigned)!ok), "r"(1 + wg)
-            : "memory");
-        if (bad) {
+            for (int j = 0; j < VPT; ++j) {
+                const int v = t + 128 * j;
+                if (v < V) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + (size_t)v * 16);
+                    const uint32_t wa[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 xh = f2mul(f2sub(bf16x2_to_f2(wa[q]), mu2), rs2);  // x_hat
+                        // x_hat * onep is rounded before the shift is added (scalar: never fused)
+                        const float2 pr = make_float2(__fmul_rn(xh.x, onep[j][q].x), __fmul_rn(xh.y, onep[j][q].y));
+                        const float2 m = f2add(pr, shift[j][q]);
+                        o[q] = pack_bf16x2(m.x, m.y);
+                    }
+                    stg16(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
+                }
+            }
             if (t == 0) {
+                mean[r] = mu;
+                rstd[r] = rs;
+            }
+        }
+        named_bar(1 + wg, 128);  // every thread is done with this block's stages
+        if (t == 0)
+            for (int jr = 0; jr < nb; ++jr) {
+                const int i = r0 + jr;
+                if (i + NST < nrows) {
+                    const int st = i % NST;
+                    mbar_arrive_expect_tx(&sm.full[wg][st], row_bytes);
+                    bulk_g2s(my_stages + (size_t)st * row_bytes, x + (size_t)(r_begin + i + NST) * D, row_bytes,
+                             &sm.full[wg][st]);
+                }
+            }
+    }
+}
+
+// ==========================================================================
+// Forward for rows of up to 8 KB (D <= 4096): one warp per token row, no
+// barriers between warps.
+//
+// A CTA takes a range of rows of one sample b, and first puts the sample's
+// onep = bf16(fp32(1 + scale)) and shift in shared memory as fp32.  Each warp
+// takes the rows lo + w, lo + w + NW, ... of the range through a private ring
+// of NS row buffers filled by 1-D bulk copies (the TMA engine); a row's 16-byte
+// vectors v = lane + 32 j are copied into registers and the stage is handed
+// back at once.  Row sums use shuffles only.  The reduction order over d: per
+// lane, vectors j ascending into two packed accumulators (even j, odd j), the
+// column pairs of a vector in order; the two accumulators, then the two halves
+// of the pairs; then a fixed xor butterfly.  It depends on D only.
+// ==========================================================================
+template <int VPL, int MAXW>
+__global__ void __launch_bounds__(MAXW * 32, 1)
+out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
+                   float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int cps, int NS) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int NW = blockDim.x >> 5;
+    const int V = D >> 3;
+    const int row_bytes = D * 2;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);             // [warps][NS]
+    float *t_onep = reinterpret_cast<float *>(smem_raw + 1024);          // [D]
+    float *t_shift = t_onep + D;                                         // [D]
+    unsigned char *ring = smem_raw + 1024 + (size_t)D * 8;               // [warps][NS][row]
+    unsigned char *my_ring = ring + (size_t)warp * NS * row_bytes;
+    uint64_t *my_full = full + warp * NS;
+
+    const int b = blockIdx.x / cps;
+    const int c = blockIdx.x % cps;
+    const int lo = (int)(((long long)c * S) / cps);
+    const int hi = (int)(((long long)(c + 1) * S) / cps);
+    const int nrows = lo + warp < hi ? (hi - 1 - lo - warp) / NW + 1 : 0;  // rows of this warp
+    const size_t row0 = (size_t)b * S + lo + warp;                        // first row; then + NW per row
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&my_full[s], 1);
+        fence_barrier_init();
+    }
+    // warm L2 with the first rows of the ring while the preceding kernel finishes
+    if (lane < NS && lane < nrows) bulk_prefetch_l2(x + (row0 + (size_t)lane * NW) * D, row_bytes);
+    __syncwarp();
+    pdl_wait();  // x and emb may come from preceding kernels
+    if (lane == 0)
+        for (int k = 0; k < NS && k < nrows; ++k) {
+            mbar_arrive_expect_tx(&my_full[k], row_bytes);
+            bulk_g2s(my_ring + (size_t)k * row_bytes, x + (row0 + (size_t)k * NW) * D, row_bytes, &my_full[k]);
+        }
+    // the sample's modulation parameters, fp32
+    const uint16_t *e = emb + (size_t)b * 2 * D;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) {
+        const uint4 sc = ldg16(e + (size_t)i * 8);
+        const uint4 sh = ldg16(e + D + (size_t)i * 8);
+        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+        const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
+        float on[8], sf[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            on[2 * q] = bf16f(bf16_bits(__fadd_rn(1.0f, bf16lo(scw[q]))));
+            on[2 * q + 1] = bf16f(bf16_bits(__fadd_rn(1.0f, bf16hi(scw[q]))));
+            sf[2 * q] = bf16lo(shw[q]);
+            sf[2 * q + 1] = bf16hi(shw[q]);
+        }
+        float4 *po = reinterpret_cast<float4 *>(t_onep + (size_t)i * 8);
+        float4 *ps = reinterpret_cast<float4 *>(t_shift + (size_t)i * 8);
+        po[0] = make_float4(on[0], on[1], on[2], on[3]);
+        po[1] = make_float4(on[4], on[5], on[6], on[7]);
+        ps[0] = make_float4(sf[0], sf[1], sf[2], sf[3]);
+        ps[1] = make_float4(sf[4], sf[5], sf[6], sf[7]);
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    const float Df = (float)D;
+    for (int k = 0; k < nrows; ++k) {
+        const size_t r = row0 + (size_t)k * NW;
+        const int st = k % NS;
+        const bool ok = mbar_wait_bounded(&my_full[st], (uint32_t)(k / NS) & 1u);
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
+            if (lane == 0) {
                 report_error(kErrOutFwdWait);
-                // let the copies this warp-group issued finish before leaving
-                const int issued = min(nrows, i + kFwdStages);
-                for (int k = i; k < issued; ++k)
-                    mbar_wait_bounded(&sm.full[wg][k % kFwdStages], (uint32_t)(k / kFwdStages) & 1u, 10000000ull);
+                // let the copies this warp issued finish before leaving
+                const int issued = min(nrows, k + NS);
+                for (int q = k; q < issued; ++q)
+                    mbar_wait_bounded(&my_full[q % NS], (uint32_t)(q / NS) & 1u, 10000000ull);
             }
             return;
         }
-        // every thread of the warp-group has read stage st: refill it
-        if (t == 0 && i + kFwdStages < nrows) {
-            mbar_arrive_expect_tx(&sm.full[wg][st], row_bytes);
-            bulk_g2s(my_stages + (size_t)st * row_bytes, x + (size_t)(r + kFwdStages) * D, row_bytes,
-                     &sm.full[wg][st]);
+        const uint4 *srow = reinterpret_cast<const uint4 *>(my_ring + (size_t)st * row_bytes);
+        uint4 xr[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int v = lane + 32 * j;
+            xr[j] = v < V ? srow[v] : make_uint4(0u, 0u, 0u, 0u);
         }
-        float tot = sm.red[wg][slot][0][0];
-        tot = __fadd_rn(tot, sm.red[wg][slot][0][1]);
-        tot = __fadd_rn(tot, sm.red[wg][slot][0][2]);
-        tot = __fadd_rn(tot, sm.red[wg][slot][0][3]);
-        const float mu = __fdiv_rn(tot, invD_num);
-
-        float s2 = 0.0f;
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = t + 128 * j;
-            if (v < V) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float c = __fsub_rn(xv[j][k], mu);
-                    s2 = __fadd_rn(s2, __fmul_rn(c, c));
-                }
-            }
+        __syncwarp();  // every lane has its part of the row: refill the stage
+        if (lane == 0 && k + NS < nrows) {
+            mbar_arrive_expect_tx(&my_full[st], row_bytes);
+            bulk_g2s(my_ring + (size_t)st * row_bytes, x + (r + (size_t)NS * NW) * D, row_bytes, &my_full[st]);
         }
-        s2 = warp_sum(s2);
-        if (lane == 0) sm.red[wg][slot][1][warp] = s2;
-        named_bar(1 + wg, 128);
-        float tq = sm.red[wg][slot][1][0];
-        tq = __fadd_rn(tq, sm.red[wg][slot][1][1]);
-        tq = __fadd_rn(tq, sm.red[wg][slot][1][2]);
-        tq = __fadd_rn(tq, sm.red[wg][slot][1][3]);
-        const float var = __fdiv_rn(tq, invD_num);
-        const float rs = __frsqrt_rn(__fadd_rn(var, eps));
-
-        uint16_t *orow = out + (size_t)r * D;
+        // mean (zero vectors past the row end add +0 and change nothing)
+        float2 s1[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = t + 128 * j;
-            if (v < V) {
-                float o[8];
+        for (int j = 0; j < VPL; ++j) {
+            s1[j & 1] = f2add(s1[j & 1], bf16x2_to_f2(xr[j].x));
+            s1[j & 1] = f2add(s1[j & 1], bf16x2_to_f2(xr[j].y));
+            s1[j & 1] = f2add(s1[j & 1], bf16x2_to_f2(xr[j].z));
+            s1[j & 1] = f2add(s1[j & 1], bf16x2_to_f2(xr[j].w));
+        }
+        const float2 t1 = f2add(s1[0], s1[1]);
+        const float mu = __fdiv_rn(warp_sum(__fadd_rn(t1.x, t1.y)), Df);
+        const float2 mu2 = f2splat(mu);
+        // variance
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            if (lane + 32 * j < V) {
+                const uint32_t wa[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float xh0 = __fmul_rn(__fsub_rn(xv[j][2 * q], mu), rs);
-                    const float xh1 = __fmul_rn(__fsub_rn(xv[j][2 * q + 1], mu), rs);
-                    o[2 * q] = __fadd_rn(__fmul_rn(xh0, bf16lo(onep[j][q])), bf16lo(shift[j][q]));
-                    o[2 * q + 1] = __fadd_rn(__fmul_rn(xh1, bf16hi(onep[j][q])), bf16hi(shift[j][q]));
+                    const float2 d = f2sub(bf16x2_to_f2(wa[q]), mu2);
+                    s2[j & 1] = f2fma(d, d, s2[j & 1]);
                 }
-                stg16(orow + (size_t)v * 8, pack8(o));
             }
         }
-        if (t == 0) {
+        const float2 t2 = f2add(s2[0], s2[1]);
+        const float var = __fdiv_rn(warp_sum(__fadd_rn(t2.x, t2.y)), Df);
+        const float rs = __frsqrt_rn(__fadd_rn(var, eps));
+        const float2 rs2 = f2splat(rs);
+        // outputs
+        uint16_t *orow = out + r * D;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int v = lane + 32 * j;
+            if (v < V) {
+                const float4 *po = reinterpret_cast<const float4 *>(t_onep + (size_t)v * 8);
+                const float4 *ps = reinterpret_cast<const float4 *>(t_shift + (size_t)v * 8);
+                const float4 oa = po[0], ob = po[1], sa = ps[0], sb = ps[1];
+                const float2 onp[4] = {make_float2(oa.x, oa.y), make_float2(oa.z, oa.w), make_float2(ob.x, ob.y),
+                                       make_float2(ob.z, ob.w)};
+                const float2 shf[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w), make_float2(sb.x, sb.y),
+                                       make_float2(sb.z, sb.w)};
+                const uint32_t wa[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 xh = f2mul(f2sub(bf16x2_to_f2(wa[q]), mu2), rs2);  // x_hat
+                    // x_hat * onep is rounded before the shift is added (scalar: never fused)
+                    const float2 pr = make_float2(__fmul_rn(xh.x, onp[q].x), __fmul_rn(xh.y, onp[q].y));
+                    const float2 m = f2add(pr, shf[q]);
+                    o[q] = pack_bf16x2(m.x, m.y);
+                }
+                stg16(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
+            }
+        }
+        if (lane == 0) {
             mean[r] = mu;
             rstd[r] = rs;
         }
     }
-    pdl_trigger();
 }
 
-template <int VPT>
+template <int VPL, int MAXW>
+static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean,
+                                      float *rstd, int B, int S, int D, float eps, cudaStream_t stream,
+                                      const DeviceInfo &dev) {
+    constexpr size_t kSmemMax = 227 * 1024;
+    auto smem_of = [&](int warps, int ns) { return 1024 + (size_t)D * 8 + (size_t)warps * ns * D * 2; };
+    // 16 warps with 2 stages each where that fits, else 8 warps with 3 (or 2)
+    int warps = 8, ns = smem_of(8, 3) <= kSmemMax ? 3 : 2;
+    if (MAXW == 16 && smem_of(16, 2) <= kSmemMax) { warps = 16; ns = 2; }
+    const size_t smem = smem_of(warps, ns);
+    auto kern = out_fwd_row_kernel<VPL, MAXW>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
+    if (err != cudaSuccess) return err;
+    // about one CTA per SM in all; every CTA within one sample
+    int cps = (dev.sm_count + B - 1) / B;
+    if (cps > S) cps = S;
+    if (cps < 1) cps = 1;
+    const long long grid = (long long)B * cps;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(warps * 32), smem, stream, x, emb, out, mean, rstd, S, D, eps,
+                      cps, ns);
+}
+
+template <int VPT, int BLK, int NST, int MINB>
 static cudaError_t launch_out_fwd_t(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean,
                                     float *rstd, int B, int S, int D, float eps, cudaStream_t stream,
                                     const DeviceInfo &dev) {
-    const size_t smem = ((sizeof(FwdSmem<VPT>) + 127) / 128) * 128 + (size_t)kWG * kFwdStages * D * 2;
-    auto kern = out_fwd_kernel<VPT>;
+    static_assert(NST == 2 * BLK && BLK <= kFwdBlock, "two blocks of rows in flight");
+    const size_t smem = ((sizeof(FwdSmem) + 127) / 128) * 128 + (size_t)kWG * NST * D * 2;
+    auto kern = out_fwd_kernel<VPT, BLK, NST, MINB>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
@@ -227,40 +453,53 @@ static cudaError_t launch_out_fwd_t(const uint16_t *x, const uint16_t *emb, uint
                       x, emb, out, mean, rstd, S, D, eps, R);
 }
 
+// Rows of up to 8 KB (D <= 4096): one warp per row.  Longer rows: the
+// warp-group kernel, with blocks of 2 rows and 4 stages (128 KB of stages).
 cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean, float *rstd,
                            int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev) {
     const int V = D / 8;
+    if (V <= 128) return launch_out_fwd_row<4, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+    if (V <= 256) return launch_out_fwd_row<8, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+    if (V <= 384) return launch_out_fwd_row<12, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+    if (V <= 512) return launch_out_fwd_row<16, 8>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
     const int vpt = (V + 127) / 128;
     switch (vpt) {
-        case 1: return launch_out_fwd_t<1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 2: return launch_out_fwd_t<2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 3: return launch_out_fwd_t<3>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 4: return launch_out_fwd_t<4>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 5: case 6: return launch_out_fwd_t<6>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        default: return launch_out_fwd_t<8>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 1: return launch_out_fwd_t<1, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 2: return launch_out_fwd_t<2, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 3: return launch_out_fwd_t<3, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 4: return launch_out_fwd_t<4, 4, 8, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 5: case 6: return launch_out_fwd_t<6, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        default: return launch_out_fwd_t<8, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
     }
 }
 
 // ==========================================================================
 // Backward, kernel 1: one CTA per (sample b, 32-token tile t).
 //
-// Thread i owns the 16-byte vectors v = i + NT j (8 columns each).  The CTA
-// walks the tile's rows in ascending s.  Per row it forms gh = g * onep and
-// xhat (bit-identical to the forward's), reduces sum(gh) and sum(gh * xhat)
-// over the row (per thread in (j, element) order, a fixed butterfly, then the
-// warps in ascending order), writes dx, and adds the products g * xhat and g
-// into per-column Neumaier accumulators: the tile's level-0 node of the tree.
-// Rows arrive through a ring of bulk copies (x row and dy row per stage).
+// Thread i owns the 16-byte vectors v = i + NT j (8 columns each).  Rows
+// arrive through a ring of bulk copies (an x row and a dy row per stage) and
+// are taken in blocks of kRowBlock rows.  Phase 1, per row in ascending s:
+// x_hat = (x - mean) * rstd (bit-identical to the forward's), g = fp32(dy),
+// gh = g * onep; the row's products g * x_hat and g go into the columns' tree
+// accumulators (the tile's level-0 node), and each warp publishes its partial
+// sums of gh and gh * x_hat (column pairs in packed fp32x2, the two halves, a
+// fixed butterfly).  After one barrier, one thread per row adds the warps'
+// partials in ascending warp order, giving c1 and c2.  Phase 2 recomputes
+// x_hat and gh from the staged rows (the same operations, so the same bits)
+// and writes dx = rstd * (gh - c1 - x_hat * c2).  The reduction order over d
+// depends on D only.
 // ==========================================================================
-constexpr int kBwdStages = 4;
+constexpr int kRowBlock = 4;    // most rows per block (a block of RB rows, NST = 2 RB stages:
+                                // two blocks of rows in flight)
 
 struct BwdSmem {
-    float red[2][2][32];      // [slot][sum gh, sum gh*xhat][warp]
+    float2 red[kRowBlock][32];  // [row of the block][warp] = (sum gh, sum gh * x_hat)
+    float2 tot[kRowBlock];      // [row of the block] = (c1, c2)
     float mu[kTile], rs[kTile];
-    uint64_t full[kBwdStages];
+    uint64_t full[2 * kRowBlock];
 };
 
-template <int VPT, int MAXNT, int MINB>
+template <int VPT, int MAXNT, int MINB, int RB, int NST>
 __global__ void __launch_bounds__(MAXNT, MINB)
 out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
                     const uint16_t *__restrict__ emb, const float *__restrict__ mean,
@@ -285,14 +524,21 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
     const size_t row0 = (size_t)b * S + s0;
 
     if (tid == 0) {
-        for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < NST; ++s) mbar_init(&sm.full[s], 1);
         fence_barrier_init();
     }
+    // warm L2 with the first rows of the ring while the preceding kernel finishes
+    // (only those: the whole tile, for every CTA at once, would not stay in L2)
+    if (tid < min(n, NST)) {
+        bulk_prefetch_l2(x + (row0 + tid) * D, row_bytes);
+        bulk_prefetch_l2(dy + (row0 + tid) * D, row_bytes);
+    }
     __syncthreads();
-    pdl_wait();
+    pdl_wait();  // mean, rstd, emb (and perhaps x, dy) come from preceding kernels
+    pdl_trigger();
 
     if (tid == 0) {
-        for (int i = 0; i < kBwdStages && i < n; ++i) {
+        for (int i = 0; i < NST && i < n; ++i) {
             unsigned char *dst = stages + (size_t)i * stage_bytes;
             mbar_arrive_expect_tx(&sm.full[i], stage_bytes);
             bulk_g2s(dst, x + (row0 + i) * D, row_bytes, &sm.full[i]);
@@ -303,111 +549,138 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         sm.mu[tid] = mean[row0 + tid];
         sm.rs[tid] = rstd[row0 + tid];
     }
-    float onep[VPT][8];
+    float2 onep[VPT][4];
     const uint16_t *e = emb + (size_t)b * 2 * D;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
         if (v < V) {
-            uint4 sc = ldg16(e + (size_t)v * 8);
-            float f[8];
-            unpack8(sc, f);
+            const uint4 sc = ldg16(e + (size_t)v * 8);
+            const uint32_t w[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) onep[j][k] = bf16f(bf16_bits(__fadd_rn(1.0f, f[k])));
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = bf16x2_to_f2(w[q]);
+                onep[j][q] = make_float2(bf16f(bf16_bits(__fadd_rn(1.0f, f.x))), bf16f(bf16_bits(__fadd_rn(1.0f, f.y))));
+            }
         } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) onep[j][k] = 0.0f;
+            for (int q = 0; q < 4; ++q) onep[j][q] = make_float2(0.0f, 0.0f);
         }
     }
     __syncthreads();
 
-    float sg_s[VPT][8], kp_s[VPT][8];  // tree node for the scale products g * xhat
-    float sg_h[VPT][8], kp_h[VPT][8];  // tree node for the shift products g
+    // Tree nodes of the scale products g * x_hat and of the shift products g, by
+    // column pair.  They start at +0 rather than at the first token: adding a
+    // value v to +0 gives v exactly with no error, so every later step is the
+    // same; only an all-zero column can differ, in the sign of its level-0 sum
+    // (+0 for -0), and its root (sum + correction) is +0 either way.
+    float2 sg_s[VPT][4], kp_s[VPT][4], sg_h[VPT][4], kp_h[VPT][4];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            sg_s[j][q] = kp_s[j][q] = sg_h[j][q] = kp_h[j][q] = make_float2(0.0f, 0.0f);
+        }
     const float Df = (float)D;
 
-    for (int i = 0; i < n; ++i) {
-        const int st = i % kBwdStages;
-        const bool ok = mbar_wait_bounded(&sm.full[st], (uint32_t)(i / kBwdStages) & 1u);
-        const unsigned char *xs = stages + (size_t)st * stage_bytes;
-        const unsigned char *gs = xs + row_bytes;
-        const float mu = sm.mu[i], rs = sm.rs[i];
-
-        float xh[VPT][8], g[VPT][8];
-        float a1 = 0.0f, a2 = 0.0f;
+    for (int r0 = 0; r0 < n; r0 += RB) {
+        const int nb = min(RB, n - r0);
+        // ---- phase 1: tree products and the row sums ----
+        bool ok = true;
+        #pragma unroll
+        for (int jr = 0; jr < RB; ++jr) if (jr < nb) {
+            const int i = r0 + jr;
+            const int st = i % NST;
+            ok = mbar_wait_bounded(&sm.full[st], (uint32_t)(i / NST) & 1u) && ok;
+            const unsigned char *xs = stages + (size_t)st * stage_bytes;
+            const unsigned char *gs = xs + row_bytes;
+            const float2 mu2 = f2splat(sm.mu[i]), rs2 = f2splat(sm.rs[i]);
+            float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = tid + NT * j;
-            if (v < V && ok) {
-                float xf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(xs + (size_t)v * 16), xf);
-                unpack8(*reinterpret_cast<const uint4 *>(gs + (size_t)v * 16), g[j]);
+            for (int j = 0; j < VPT; ++j) {
+                const int v = tid + NT * j;
+                if (v < V && ok) {
+                    const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
+                    const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
+                    const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
+                    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    xh[j][k] = __fmul_rn(__fsub_rn(xf[k], mu), rs);
-                    const float gh = __fmul_rn(g[j][k], onep[j][k]);
-                    a1 = __fadd_rn(a1, gh);
-                    a2 = __fadd_rn(a2, __fmul_rn(gh, xh[j][k]));
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 g2 = bf16x2_to_f2(ga[q]);
+                        const float2 xh = f2mul(f2sub(bf16x2_to_f2(xa[q]), mu2), rs2);
+                        const float2 gh = f2mul(g2, onep[j][q]);
+                        a1 = f2add(a1, gh);
+                        a2 = f2fma(gh, xh, a2);
+                        // the token product g * x_hat is rounded before it enters the tree
+                        const float2 ps = make_float2(__fmul_rn(g2.x, xh.x), __fmul_rn(g2.y, xh.y));
+                        twosum2(sg_s[j][q], kp_s[j][q], ps);
+                        twosum2(sg_h[j][q], kp_h[j][q], g2);
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) { xh[j][k] = 0.0f; g[j][k] = 0.0f; }
             }
-        }
-        a1 = warp_sum(a1);
-        a2 = warp_sum(a2);
-        const int slot = i & 1;
-        if (lane == 0) {
-            sm.red[slot][0][warp] = a1;
-            sm.red[slot][1][warp] = a2;
+            const float2 part = warp_sum2(make_float2(__fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y)));
+            if (lane == 0) sm.red[jr][warp] = part;
         }
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 report_error(kErrOutBwdWait);
-                const int issued = min(n, i + kBwdStages);
-                for (int k = i; k < issued; ++k)
-                    mbar_wait_bounded(&sm.full[k % kBwdStages], (uint32_t)(k / kBwdStages) & 1u, 10000000ull);
+                // let the copies this CTA issued finish before leaving
+                const int issued = min(n, r0 + NST);
+                for (int k = r0; k < issued; ++k)
+                    mbar_wait_bounded(&sm.full[k % NST], (uint32_t)(k / NST) & 1u, 10000000ull);
             }
             return;
         }
-        if (tid == 0 && i + kBwdStages < n) {
-            unsigned char *dst = stages + (size_t)st * stage_bytes;
-            mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
-            bulk_g2s(dst, x + (row0 + i + kBwdStages) * D, row_bytes, &sm.full[st]);
-            bulk_g2s(dst + row_bytes, dy + (row0 + i + kBwdStages) * D, row_bytes, &sm.full[st]);
+        if (tid < nb) {
+            float2 c = sm.red[tid][0];
+            for (int w = 1; w < nwarps; ++w) c = f2add(c, sm.red[tid][w]);
+            sm.tot[tid] = make_float2(__fdiv_rn(c.x, Df), __fdiv_rn(c.y, Df));
         }
-        float c1 = sm.red[slot][0][0], c2 = sm.red[slot][1][0];
-        for (int w = 1; w < nwarps; ++w) {
-            c1 = __fadd_rn(c1, sm.red[slot][0][w]);
-            c2 = __fadd_rn(c2, sm.red[slot][1][w]);
-        }
-        c1 = __fdiv_rn(c1, Df);
-        c2 = __fdiv_rn(c2, Df);
-
-        uint16_t *drow = dx + (row0 + i) * D;
+        __syncthreads();
+        // ---- phase 2: dx ----
+        #pragma unroll
+        for (int jr = 0; jr < RB; ++jr) if (jr < nb) {
+            const int i = r0 + jr;
+            const unsigned char *xs = stages + (size_t)(i % NST) * stage_bytes;
+            const unsigned char *gs = xs + row_bytes;
+            const float2 mu2 = f2splat(sm.mu[i]), rs2 = f2splat(sm.rs[i]);
+            const float2 c = sm.tot[jr];
+            const float2 nc1 = f2splat(-c.x), nc2 = f2splat(-c.y);
+            uint16_t *drow = dx + (row0 + i) * D;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = tid + NT * j;
-            if (v < V) {
-                float o[8];
+            for (int j = 0; j < VPT; ++j) {
+                const int v = tid + NT * j;
+                if (v < V) {
+                    const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
+                    const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
+                    const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
+                    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
+                    uint32_t o[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float gh = __fmul_rn(g[j][k], onep[j][k]);
-                    o[k] = __fmul_rn(rs, __fsub_rn(__fsub_rn(gh, c1), __fmul_rn(xh[j][k], c2)));
-                    const float ps = __fmul_rn(g[j][k], xh[j][k]);
-                    if (i == 0) {
-                        sg_s[j][k] = ps; kp_s[j][k] = 0.0f;
-                        sg_h[j][k] = g[j][k]; kp_h[j][k] = 0.0f;
-                    } else {
-                        neumaier(sg_s[j][k], kp_s[j][k], ps);
-                        neumaier(sg_h[j][k], kp_h[j][k], g[j][k]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 xh = f2mul(f2sub(bf16x2_to_f2(xa[q]), mu2), rs2);
+                        const float2 gh = f2mul(bf16x2_to_f2(ga[q]), onep[j][q]);
+                        const float2 d = f2mul(f2fma(xh, nc2, f2add(gh, nc1)), rs2);
+                        o[q] = pack_bf16x2(d.x, d.y);
                     }
+                    stg16(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
                 }
-                stg16(drow + (size_t)v * 8, pack8(o));
             }
         }
+        __syncthreads();  // every thread is done with this block's stages
+        if (tid == 0)
+            for (int jr = 0; jr < nb; ++jr) {
+                const int i = r0 + jr;
+                if (i + NST < n) {
+                    const int st = i % NST;
+                    unsigned char *dst = stages + (size_t)st * stage_bytes;
+                    mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
+                    bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                    bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                }
+            }
     }
-    pdl_trigger();
-    // level-0 node of this tile
+    // level-0 node of this tile: scale half at columns [0, D), shift half at [D, 2D)
     const int H = 2 * D;
     float *ps = ws_sig + ((size_t)b * T + tile) * H;
     float *pk = ws_kap + ((size_t)b * T + tile) * H;
@@ -416,14 +689,14 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         const int v = tid + NT * j;
         if (v < V) {
             const size_t c = (size_t)v * 8;
-            stg16f(ps + c, make_float4(sg_s[j][0], sg_s[j][1], sg_s[j][2], sg_s[j][3]));
-            stg16f(ps + c + 4, make_float4(sg_s[j][4], sg_s[j][5], sg_s[j][6], sg_s[j][7]));
-            stg16f(pk + c, make_float4(kp_s[j][0], kp_s[j][1], kp_s[j][2], kp_s[j][3]));
-            stg16f(pk + c + 4, make_float4(kp_s[j][4], kp_s[j][5], kp_s[j][6], kp_s[j][7]));
-            stg16f(ps + D + c, make_float4(sg_h[j][0], sg_h[j][1], sg_h[j][2], sg_h[j][3]));
-            stg16f(ps + D + c + 4, make_float4(sg_h[j][4], sg_h[j][5], sg_h[j][6], sg_h[j][7]));
-            stg16f(pk + D + c, make_float4(kp_h[j][0], kp_h[j][1], kp_h[j][2], kp_h[j][3]));
-            stg16f(pk + D + c + 4, make_float4(kp_h[j][4], kp_h[j][5], kp_h[j][6], kp_h[j][7]));
+            stg16f(ps + c, make_float4(sg_s[j][0].x, sg_s[j][0].y, sg_s[j][1].x, sg_s[j][1].y));
+            stg16f(ps + c + 4, make_float4(sg_s[j][2].x, sg_s[j][2].y, sg_s[j][3].x, sg_s[j][3].y));
+            stg16f(pk + c, make_float4(kp_s[j][0].x, kp_s[j][0].y, kp_s[j][1].x, kp_s[j][1].y));
+            stg16f(pk + c + 4, make_float4(kp_s[j][2].x, kp_s[j][2].y, kp_s[j][3].x, kp_s[j][3].y));
+            stg16f(ps + D + c, make_float4(sg_h[j][0].x, sg_h[j][0].y, sg_h[j][1].x, sg_h[j][1].y));
+            stg16f(ps + D + c + 4, make_float4(sg_h[j][2].x, sg_h[j][2].y, sg_h[j][3].x, sg_h[j][3].y));
+            stg16f(pk + D + c, make_float4(kp_h[j][0].x, kp_h[j][0].y, kp_h[j][1].x, kp_h[j][1].y));
+            stg16f(pk + D + c + 4, make_float4(kp_h[j][2].x, kp_h[j][2].y, kp_h[j][3].x, kp_h[j][3].y));
         }
     }
 }
@@ -478,7 +751,7 @@ struct FoldSmem {
 
 // one group of the fold: Neumaier sum of the children's sums in ascending
 // order (compensation c), children's corrections added in ascending order;
-// node = (sum, c + corrections)
+// node = (sum, c + corrections).  Children are loaded eight at a time.
 __device__ __forceinline__ void fold_group(const float *sig, const float *kap, size_t stride, int count,
                                            float &out_s, float &out_k) {
     float s = 0.0f, c = 0.0f, k = 0.0f;
@@ -496,7 +769,7 @@ __device__ __forceinline__ void fold_group(const float *sig, const float *kap, s
                 s = vs[0];
                 k = vk[0];
             } else if (i0 + q < count) {
-                neumaier(s, c, vs[q]);
+                twosum(s, c, vs[q]);
                 k = __fadd_rn(k, vk[q]);
             }
         }
@@ -505,7 +778,9 @@ __device__ __forceinline__ void fold_group(const float *sig, const float *kap, s
     out_k = __fadd_rn(c, k);
 }
 
-__global__ void __launch_bounds__(1024)
+constexpr int kFoldWarps = 8;
+
+__global__ void __launch_bounds__(kFoldWarps * 32)
 tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_kap, float *__restrict__ out,
                  int T, int H) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -578,7 +853,7 @@ __global__ void zero_kernel(float *__restrict__ p, size_t n) {
 static cudaError_t launch_fold(const float *sig, const float *kap, float *out, int B, int T, int H,
                                cudaStream_t stream, const DeviceInfo &dev) {
     const int n1 = (T + kTile - 1) / kTile;
-    const int warps = T == 1 ? 1 : min(32, n1);
+    const int warps = T == 1 ? 1 : min(kFoldWarps, n1);
     const size_t smem = sizeof(FoldSmem);
     cudaError_t err = ensure_smem_attr((const void *)tree_fold_kernel, smem, dev);
     if (err != cudaSuccess) return err;
@@ -591,20 +866,24 @@ static cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream) {
     return launch_pdl(zero_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, p, n);
 }
 
-template <int VPT, int MAXNT, int MINB>
+template <int VPT, int MAXNT, int MINB, int RB, int NST>
 static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                                     const float *rstd, uint16_t *dx, float *sig, float *kap, int B, int S, int D,
                                     int T, cudaStream_t stream, const DeviceInfo &dev) {
+    static_assert(NST == 2 * RB && RB <= kRowBlock, "two blocks of rows in flight");
     const int V = D / 8;
     const int nt = ((V + VPT - 1) / VPT + 31) / 32 * 32;
-    const size_t smem = ((sizeof(BwdSmem) + 127) / 128) * 128 + (size_t)kBwdStages * 4 * D;
-    auto kern = out_bwd_tile_kernel<VPT, MAXNT, MINB>;
+    const size_t smem = ((sizeof(BwdSmem) + 127) / 128) * 128 + (size_t)NST * 4 * D;
+    auto kern = out_bwd_tile_kernel<VPT, MAXNT, MINB, RB, NST>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(T, B), dim3(nt), smem, stream, dy, x, emb, mean, rstd, dx, sig, kap,
                       S, D, T);
 }
 
+// Stages of up to 12 KB (D <= 3072): two CTAs of <= 384 threads per SM, blocks
+// of 4 rows, 8 stages; up to 16 KB: one CTA per SM, the same ring; longer
+// rows: blocks of 2 rows and 4 stages (at most 128 KB of stages).
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
                            cudaStream_t stream, const DeviceInfo &dev) {
@@ -616,11 +895,11 @@ cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t
     const int V = D / 8;
     cudaError_t err;
     if (V <= 384)
-        err = launch_out_bwd_t<1, 384, 2>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<1, 384, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     else if (V <= 512)
-        err = launch_out_bwd_t<1, 512, 1>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<1, 512, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     else
-        err = launch_out_bwd_t<2, 512, 1>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<2, 512, 1, 2, 4>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
 }

@@ -9,14 +9,36 @@
 //
 // Layout: W [2D, D] bf16 row-major (row n = output feature n), temb, u [B, D]
 // bf16, emb [B, 2D] bf16, d_emb [B, 2D] fp32, dW [2D, D], db [2D].
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace adaln {
 
 // --------------------------------------------------------------------------
-// u = bf16(silu(temb)): 8 elements per thread
+// SiLU as a lookup: a bf16 input has 65536 values, so u = bf16(silu(t)) is
+// tabulated once per device by silu_table_kernel (silu_bf16 on every bit
+// pattern, the same bits as computing it in place).  silu_bf16 recomputes in
+// fp64 near a bf16 rounding tie, and fp64 is slow on this GPU: one warp that
+// takes that branch stalls for microseconds, so the hot kernels look the
+// value up instead (128 KB, cached in L1 after first use).
 // --------------------------------------------------------------------------
+static __device__ uint16_t g_silu_tab[65536];
+
+__global__ void __launch_bounds__(256) silu_table_kernel() {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < 65536) g_silu_tab[i] = silu_bf16((uint16_t)i);
+}
+
+// u for one packed bf16x2 word
+__device__ __forceinline__ uint32_t silu_word(uint32_t w) {
+    const uint32_t lo = __ldg(&g_silu_tab[w & 0xFFFFu]);
+    const uint32_t hi = __ldg(&g_silu_tab[w >> 16]);
+    return lo | (hi << 16);
+}
+
+// u = bf16(silu(temb)): 8 elements per thread
 __global__ void __launch_bounds__(256) silu_kernel(const uint16_t *__restrict__ temb, uint16_t *__restrict__ u,
                                                    long long n8) {
     pdl_wait();
@@ -24,25 +46,29 @@ __global__ void __launch_bounds__(256) silu_kernel(const uint16_t *__restrict__ 
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const uint4 t = ldg16(temb + i * 8);
-    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint16_t lo = silu_bf16((uint16_t)(w[q] & 0xFFFFu));
-        const uint16_t hi = silu_bf16((uint16_t)(w[q] >> 16));
-        o[q] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    stg16(u + i * 8, make_uint4(o[0], o[1], o[2], o[3]));
+    stg16(u + i * 8, make_uint4(silu_word(t.x), silu_word(t.y), silu_word(t.z), silu_word(t.w)));
 }
 
 // --------------------------------------------------------------------------
-// emb[b,n] = bf16(sum_k u[b,k] W[n,k] + bias[n]).  One warp per output row n.
-// Lane l accumulates the 16-byte vectors v = l, l+32, l+64, ... of the row in
-// ascending order (8 products each, in element order; each product of two
-// bf16 is exact in fp32, so the fused multiply-add rounds once per term), then
-// the lanes combine by a fixed xor butterfly.  The samples are staged in
-// shared memory BC at a time; the order per (b, n) never changes.
+// The projection's summation order, shared by both kernels below:
+// emb[b,n] = bf16(sum_k u[b,k] W[n,k] + bias[n]), one warp per output row n.
+// Lane l takes the 16-byte vectors v = l, l+32, l+64, ... of the row in
+// ascending order; within a vector the element pairs (0,1), (2,3), (4,5),
+// (6,7) in order, even elements into one fp32 accumulator and odd ones into
+// another (one packed fused multiply-add per pair; each product of two bf16 is
+// exact in fp32, so every term is rounded once).  Then the two accumulators are
+// added, the lanes combine by a fixed xor butterfly, and the bias is added in
+// fp32 before the one bf16 rounding.  The order depends on D only.
 // --------------------------------------------------------------------------
+__device__ __forceinline__ float2 dot_pairs(uint4 w, float2 u0, float2 u1, float2 u2, float2 u3, float2 acc) {
+    acc = f2fma(u0, bf16x2_to_f2(w.x), acc);
+    acc = f2fma(u1, bf16x2_to_f2(w.y), acc);
+    acc = f2fma(u2, bf16x2_to_f2(w.z), acc);
+    acc = f2fma(u3, bf16x2_to_f2(w.w), acc);
+    return acc;
+}
+
+// emb for up to BC samples at a time; samples staged in shared memory as bf16.
 constexpr int kFwdVL = 12;  // W vectors per lane held in registers (one row of D = 3072)
 
 template <int BC>
@@ -74,9 +100,9 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
         const int nb = min(BC, B - b0);
         for (int i = threadIdx.x; i < nb * V; i += blockDim.x) us[i] = ldg16(u + (size_t)b0 * D + (size_t)i * 8);
         __syncthreads();
-        float acc[BC];
+        float2 acc[BC];
 #pragma unroll
-        for (int b = 0; b < BC; ++b) acc[b] = 0.0f;
+        for (int b = 0; b < BC; ++b) acc[b] = make_float2(0.0f, 0.0f);
         for (int v0 = 0; v0 < V; v0 += 32 * kFwdVL) {
             if (!one_chunk && (v0 > 0 || b0 > 0)) {
 #pragma unroll
@@ -89,15 +115,12 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
             for (int q = 0; q < kFwdVL; ++q) {
                 const int v = v0 + lane + 32 * q;
                 if (v < V) {
-                    float w[8];
-                    unpack8(wv[q], w);
 #pragma unroll
                     for (int b = 0; b < BC; ++b) {
                         if (b < nb) {
-                            float x[8];
-                            unpack8(us[b * V + v], x);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[b] = __fmaf_rn(x[e], w[e], acc[b]);
+                            const uint4 x = us[b * V + v];
+                            acc[b] = dot_pairs(wv[q], bf16x2_to_f2(x.x), bf16x2_to_f2(x.y), bf16x2_to_f2(x.z),
+                                               bf16x2_to_f2(x.w), acc[b]);
                         }
                     }
                 }
@@ -106,7 +129,7 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
 #pragma unroll
         for (int b = 0; b < BC; ++b) {
             if (b < nb) {
-                const float tot = warp_sum(acc[b]);
+                const float tot = warp_sum(__fadd_rn(acc[b].x, acc[b].y));
                 if (lane == 0 && live) emb[(size_t)(b0 + b) * N + n] = bf16_bits(__fadd_rn(tot, bn));
             }
         }
@@ -116,20 +139,130 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
 }
 
 // --------------------------------------------------------------------------
-// Backward, kernel 1: one CTA per (k-chunk of 256 columns, slab of 384 rows).
+// The same projection for up to kStreamMaxB samples in one kernel, SiLU
+// included.  Every CTA computes u = bf16(silu(temb)) for all samples into
+// shared memory (as fp32; it also writes its share of u), while the first W
+// row of each warp is already in flight: warp gw (global index, NW warps in
+// all) takes rows n = gw, gw + NW, ..., two at a time for up to 2 samples (one
+// otherwise), each lane loading its vectors v = lane + 32 j of the rows into
+// registers (16-byte loads) before any arithmetic.  The order of the terms is the one above, so both kernels
+// give the same bits.
+// --------------------------------------------------------------------------
+constexpr int kStreamMaxB = 8;
+constexpr int kStreamWarps = 8;
+constexpr int kStreamVL = 12;  // W vectors per lane and row held in registers (D <= 3072)
+
+static __device__ unsigned g_proj_err;  // device-side error word of this file's kernels
+
+template <int BC>
+__global__ void __launch_bounds__(kStreamWarps * 32, 2)
+proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__restrict__ W,
+                       const uint16_t *__restrict__ bias, uint16_t *__restrict__ emb, uint16_t *__restrict__ u,
+                       int B, int D) {
+    extern __shared__ __align__(128) float uf[];  // [B][D] fp32
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = 2 * D;
+    const int V = D >> 3;
+
+    const int NW = gridDim.x * kStreamWarps;
+    const int gw = blockIdx.x * kStreamWarps + warp;
+    const int nrows = gw < N ? (N - 1 - gw) / NW + 1 : 0;  // rows of this warp
+
+    pdl_wait();  // temb, W, bias may come from preceding kernels
+    uint4 wa[kStreamVL], wb[kStreamVL];
+    auto load_row = [&](uint4(&w)[kStreamVL], int n) {
+#pragma unroll
+        for (int j = 0; j < kStreamVL; ++j) {
+            const int v = lane + 32 * j;
+            w[j] = v < V ? ldg16(W + (size_t)n * D + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    constexpr int R = BC <= 2 ? 2 : 1;  // rows in flight per warp (registers)
+    if (nrows > 0) load_row(wa, gw);
+    // the bias of this warp's rows, lane k holding row k (raw bits: converted at use)
+    const uint16_t bias_raw = lane < nrows ? bias[gw + lane * NW] : (uint16_t)0;
+
+    // u = bf16(silu(temb)) for every sample; this CTA stores vectors i = blockIdx.x (mod gridDim.x)
+    for (int i = threadIdx.x; i < B * V; i += blockDim.x) {
+        const uint4 t = ldg16(temb + (size_t)i * 8);
+        const uint32_t o[4] = {silu_word(t.x), silu_word(t.y), silu_word(t.z), silu_word(t.w)};
+        float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)i * 8);
+        dst[0] = make_float4(bf16lo(o[0]), bf16hi(o[0]), bf16lo(o[1]), bf16hi(o[1]));
+        dst[1] = make_float4(bf16lo(o[2]), bf16hi(o[2]), bf16lo(o[3]), bf16hi(o[3]));
+        if (i % gridDim.x == blockIdx.x) stg16(u + (size_t)i * 8, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+    if (R == 2 && nrows > 1) load_row(wb, gw + NW);
+    __syncthreads();
+    pdl_trigger();
+
+    auto row_dot = [&](const uint4(&w)[kStreamVL], float2(&acc)[BC]) {
+#pragma unroll
+        for (int b = 0; b < BC; ++b) acc[b] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < kStreamVL; ++j) {
+            const int v = lane + 32 * j;
+            if (v < V) {
+#pragma unroll
+                for (int b = 0; b < BC; ++b) {
+                    if (b < B) {
+                        const float4 *up = reinterpret_cast<const float4 *>(uf + (size_t)b * D + (size_t)v * 8);
+                        const float4 ua = up[0], ub = up[1];
+                        acc[b] = dot_pairs(w[j], make_float2(ua.x, ua.y), make_float2(ua.z, ua.w),
+                                           make_float2(ub.x, ub.y), make_float2(ub.z, ub.w), acc[b]);
+                    }
+                }
+            }
+        }
+    };
+    auto finish = [&](const float2(&acc)[BC], int k) {
+        const int n = gw + k * NW;
+        const float bk = bf16f((uint16_t)__shfl_sync(0xFFFFFFFFu, (uint32_t)bias_raw, k & 31));
+        const float bn = k < 32 ? bk : bf16f(bias[n]);
+#pragma unroll
+        for (int b = 0; b < BC; ++b) {
+            if (b < B) {
+                const float tot = warp_sum(__fadd_rn(acc[b].x, acc[b].y));
+                if (lane == 0) emb[(size_t)b * N + n] = bf16_bits(__fadd_rn(tot, bn));
+            }
+        }
+    };
+    if (R == 2) {
+        for (int k = 0; k < nrows; k += 2) {
+            float2 acc_a[BC], acc_b[BC];
+            row_dot(wa, acc_a);
+            if (k + 1 < nrows) row_dot(wb, acc_b);
+            // the next two rows go in flight before the sums of these two
+            if (k + 2 < nrows) load_row(wa, gw + (k + 2) * NW);
+            if (k + 3 < nrows) load_row(wb, gw + (k + 3) * NW);
+            finish(acc_a, k);
+            if (k + 1 < nrows) finish(acc_b, k + 1);
+        }
+    } else {
+        for (int k = 0; k < nrows; ++k) {
+            float2 acc_a[BC];
+            row_dot(wa, acc_a);
+            if (k + 1 < nrows) load_row(wa, gw + (k + 1) * NW);
+            finish(acc_a, k);
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Backward, kernel 1: one CTA per (k-chunk of 256 columns, slab of 256 rows).
 //
 // Warp w takes the slab's rows n = n0 + w + 8 i (i ascending), lane l the 8
-// columns k = k0 + 8 l .. +7.  For the samples of the current chunk it adds
-// e[b,n] * W[n,k] into fp32 partials (each product exact), then the 8 warps'
-// partials are added in ascending warp order and written per slab:
-// ws[slab][b][k].  The slab size, and so this order, depends on D only.
-// With WITH_W (all samples in one chunk) it also produces dW and db for its
-// tile: acc = (accumulate ? acc_in : +0), then + e[b,n] * u[b,k] for b
-// ascending, one rounding per add.
+// columns k = k0 + 8 l .. +7; each warp keeps kPre rows of W in flight.  For
+// the samples of the current chunk it adds e[b,n] * W[n,k] into fp32 partials
+// (each product exact), then the 8 warps' partials are added in ascending warp
+// order and written per slab: ws[slab][b][k].  The slab size, and so this
+// order, depends on D only.  With WITH_W (all samples in one chunk) it also
+// produces dW and db for its tile: acc = (accumulate ? acc_in : +0), then
+// + e[b,n] * u[b,k] for b ascending, one rounding per add.
 // --------------------------------------------------------------------------
-constexpr int kSlabRows = kProjSlabRows;        // 384
-constexpr int kRowsPerWarp = kSlabRows / 8;     // 48
-constexpr int kPre = 4;                         // rows loaded ahead per warp
+constexpr int kSlabRows = kProjSlabRows;        // 256
+constexpr int kRowsPerWarp = kSlabRows / 8;     // 32
+constexpr int kPreMax = 16;                      // rows of W in flight per warp (up to 2 samples)
 
 template <int BC>
 struct SlabSmem {
@@ -138,7 +271,7 @@ struct SlabSmem {
 };
 
 template <int BC, bool WITH_W>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, const uint16_t *__restrict__ W,
                      float *__restrict__ dW_acc, float *__restrict__ db_acc, uint16_t *__restrict__ dW,
                      uint16_t *__restrict__ db, int accumulate, float *__restrict__ ws, int B, int D) {
@@ -149,15 +282,21 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int N = 2 * D;
-    const int V = D >> 3;
     const int n0 = slab * kSlabRows;
     const int kv = kchunk * 32 + lane;
-    const bool live_k = kv < V;
+    const bool live_k = kv < (D >> 3);
     const int col = kv * 8;
-    const int cnt = min(kRowsPerWarp, (N - n0) / 8);  // rows per warp, equal for all warps
+    const int cnt = min(kRowsPerWarp, (N - n0) / 8);  // rows per warp, equal for all warps (N % 16 == 0)
     const bool want_dw = WITH_W && (dW_acc != nullptr || dW != nullptr);
     const bool want_db = WITH_W && (db_acc != nullptr || db != nullptr) && kchunk == 0 && lane == 0;
+    constexpr int kPre = BC <= 2 ? kPreMax : kPreMax / 2;  // fewer rows in flight where more samples need registers
 
+    // warm L2 with this warp's rows of W (an input of the call) while the preceding kernel finishes
+    if (B > 0 && lane < cnt) {
+        const int kv0 = kchunk * 32;
+        const int nvec = min(32, (D >> 3) - kv0);  // vectors of this k-chunk
+        bulk_prefetch_l2(W + (size_t)(n0 + warp + 8 * lane) * D + kv0 * 8, (uint32_t)nvec * 16);
+    }
     pdl_wait();
 
     for (int b0 = 0; b0 < B || (WITH_W && b0 == 0); b0 += BC) {
@@ -190,6 +329,7 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
 #pragma unroll
             for (int p = 0; p < kPre; ++p) {
                 const int n = n0 + warp + 8 * (i0 + p);
+                wv[p] = make_uint4(0u, 0u, 0u, 0u);  // W is not read without samples
                 if (i0 + p < cnt && live_k && nb > 0) wv[p] = ldg16(W + (size_t)n * D + col);
             }
 #pragma unroll
@@ -199,7 +339,7 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                     const int r = warp + 8 * i;
                     const int n = n0 + r;
                     float w[8];
-                    unpack8(nb > 0 ? wv[p] : make_uint4(0u, 0u, 0u, 0u), w);  // W is not read without samples
+                    unpack8(wv[p], w);
 #pragma unroll
                     for (int b = 0; b < BC; ++b) {
                         if (b < nb) {
@@ -269,6 +409,8 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
 // --------------------------------------------------------------------------
 // Backward, kernel 2: d_temb[b,k] = bf16((sum over slabs, ascending) * silu'(t))
 // --------------------------------------------------------------------------
+constexpr int kMaxSlabs = 2 * kMaxD / kProjSlabRows;  // 64
+
 __global__ void __launch_bounds__(256)
 proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__ temb, uint16_t *__restrict__ d_temb,
                       int B, int D, int nslab) {
@@ -276,8 +418,14 @@ proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
     if (i < BD) {
-        float tot = ws[i];
-        for (int s = 1; s < nslab; ++s) tot = __fadd_rn(tot, ws[(size_t)s * BD + i]);
+        // all partials are loaded before the first add (nslab <= kMaxSlabs)
+        float part[kMaxSlabs];
+#pragma unroll
+        for (int s = 0; s < kMaxSlabs; ++s) part[s] = s < nslab ? ws[(size_t)s * BD + i] : 0.0f;
+        float tot = part[0];
+#pragma unroll
+        for (int s = 1; s < kMaxSlabs; ++s)
+            if (s < nslab) tot = __fadd_rn(tot, part[s]);
         d_temb[i] = bf16_bits(__fmul_rn(tot, dsilu_f32(bf16f(temb[i]))));
     }
     pdl_trigger();
@@ -378,15 +526,67 @@ static cudaError_t launch_proj_fwd_gemv(const uint16_t *W, const uint16_t *bias,
     return launch_pdl(kern, dim3((2 * D + 7) / 8), dim3(256), smem, stream, W, bias, u, emb, B, D);
 }
 
+template <int BC>
+static cudaError_t launch_proj_fwd_stream(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
+                                          uint16_t *emb, uint16_t *u, int B, int D, size_t smem, cudaStream_t stream,
+                                          const DeviceInfo &dev) {
+    auto kern = proj_fwd_stream_kernel<BC>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStreamWarps * 32, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    const int N = 2 * D;
+    int grid = dev.sm_count * per_sm;
+    const int need = (N + kStreamWarps - 1) / kStreamWarps;
+    if (grid > need) grid = need;
+    return launch_pdl(kern, dim3(grid), dim3(kStreamWarps * 32), smem, stream, temb, W, bias, emb, u, B, D);
+}
+
+// The SiLU table of the current device, filled by its first call: launched on
+// the caller's stream, which is then synchronized once, so that calls on other
+// streams never read the table before it is complete.
+static std::mutex g_tab_mu;
+static bool g_tab_ready[64];
+
+static cudaError_t ensure_silu_table(cudaStream_t stream, const DeviceInfo &dev) {
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_tab_mu);
+    if (g_tab_ready[dev.device]) return cudaSuccess;
+    silu_table_kernel<<<65536 / 256, 256, 0, stream>>>();
+    cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err == cudaSuccess) g_tab_ready[dev.device] = true;
+    return err;
+}
+
+// Up to kStreamMaxB samples and D <= 3072: the fused kernel; otherwise the
+// SiLU kernel, then the chunked GEMV.
 cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
                             uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
+    if (B == 0) return cudaSuccess;
+    cudaError_t terr = ensure_silu_table(stream, dev);
+    if (terr != cudaSuccess) return terr;
+    const size_t smem = (size_t)B * D * 4;
+    if (B <= kStreamMaxB && D / 8 <= 32 * kStreamVL) {
+        if (B == 1) return launch_proj_fwd_stream<1>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+        if (B == 2) return launch_proj_fwd_stream<2>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+        if (B <= 4) return launch_proj_fwd_stream<4>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+        return launch_proj_fwd_stream<8>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+    }
     const long long n8 = (long long)B * D / 8;
     cudaError_t err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
     if (err != cudaSuccess) return err;
-    if (B == 1) return launch_proj_fwd_gemv<1>(W, bias, u, emb, B, D, stream, dev);
-    if (B == 2) return launch_proj_fwd_gemv<2>(W, bias, u, emb, B, D, stream, dev);
     if (B <= 4) return launch_proj_fwd_gemv<4>(W, bias, u, emb, B, D, stream, dev);
     return launch_proj_fwd_gemv<8>(W, bias, u, emb, B, D, stream, dev);
+}
+
+int read_and_clear_proj_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_proj_err, sizeof(v)) != cudaSuccess) return -1;
+    if (v != 0 && cudaMemcpyToSymbol(g_proj_err, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    return (int)v;
 }
 
 template <int BC, bool WITH_W>

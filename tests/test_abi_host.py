@@ -60,7 +60,7 @@ def test_workspace_sizes(L):
     assert L.adaln_out_bwd_workspace_bytes(0, 33, D) == 0
     assert L.adaln_out_bwd_workspace_bytes(2, 0, D) == 0
     assert L.token_sum_tree_workspace_bytes(1, 1, 4) == 256  # 32 bytes, rounded to 256
-    assert L.adaln_proj_bwd_workspace_bytes(2, D) == 16 * 2 * 3072 * 4
+    assert L.adaln_proj_bwd_workspace_bytes(2, D) == 24 * 2 * 3072 * 4  # ceil(2D / 256) slabs
     assert L.adaln_proj_bwd_workspace_bytes(0, D) == 0
 
 

@@ -1,0 +1,175 @@
+"""Bytewise batch invariance of the whole fwd+bwd path on the GPU.
+
+The pages' protocol (RL-Kernel PR 538, "Prior art & reuse decision"): a
+singleton compared with every row of B = 64/257/2048, three seeds, B = 2 vs
+B = 1 at long sequences, and a workload run in five chunkings.  Every per-sample
+output (emb, u, out, mean, rstd, dx, d_emb, d_temb) of sample b in a batch
+must have the bytes of the same sample run alone; dW and db summed over a
+workload in chunks (accumulating into fp32) must have the bytes of one call.
+"""
+
+from __future__ import annotations
+
+import pytest
+import torch
+
+from invariant_dit_adaln_gb300 import binding
+from gpu_util import lib, run_step
+
+pytestmark = pytest.mark.gpu
+
+PER_SAMPLE = ("emb", "u", "out", "mean", "rstd", "dx", "d_emb", "d_temb")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib()
+    yield
+    assert binding.device_error() == 0
+
+
+def _device_inputs(n, S, D, seed, outlier_frac=0.0):
+    """Seeded synthetic inputs generated on the device (these tests compare the
+    GPU with itself, and the host generator would take minutes at these
+    sizes): x, dy, temb ~ N(0, 1) from torch's Philox generator, rounded to
+    bf16; W, b ~ N(0, 0.02^2); optionally floor(frac*n*S) token rows of x and
+    dy scaled by 50 in fp32 before the rounding."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn((n, S, D), generator=g, device="cuda")
+    dy = torch.randn((n, S, D), generator=g, device="cuda")
+    k = int(outlier_frac * n * S)
+    if k:
+        rows = torch.randperm(n * S, generator=g, device="cuda")[:k]
+        x.view(n * S, D)[rows] *= 50
+        dy.view(n * S, D)[rows] *= 50
+    temb = torch.randn((n, D), generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn((2 * D, D), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    b = (torch.randn((2 * D,), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    return {"x": x.to(torch.bfloat16), "dy": dy.to(torch.bfloat16), "temb": temb, "W": W, "b": b}
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+def _compare_rows(batch, single, b, what):
+    for k in PER_SAMPLE:
+        if not torch.equal(_bits(batch[k][b:b + 1]), _bits(single[k])):
+            raise AssertionError(f"{what}: {k} of sample {b} differs from the sample run alone")
+
+
+def _one(dev, b):
+    return {k: (v if k in ("W", "b") else v[b:b + 1]) for k, v in dev.items()}
+
+
+def test_projection_is_M_invariant_across_batch_sizes():
+    """emb rows are bit-identical for B = 1 .. 64, across the switch between
+    the fused streaming kernel (B <= 8) and the chunked kernel (B > 8)."""
+    D = 3072
+    big = _device_inputs(64, 1, D, seed=3)
+    W, b = big["W"], big["b"]
+    ref, uref = binding.adaln_proj_fwd(big["temb"], W, b)
+    for B in [1, 2, 3, 4, 5, 7, 8, 9, 16, 33]:
+        e, u = binding.adaln_proj_fwd(big["temb"][:B], W, b)
+        assert torch.equal(_bits(e), _bits(ref[:B])), B
+        assert torch.equal(_bits(u), _bits(uref[:B])), B
+
+
+@pytest.mark.parametrize("seed", [0, 127, 2026])
+@pytest.mark.parametrize("S", [31, 32, 33])
+@pytest.mark.parametrize("B", [64, 257])
+def test_every_row_matches_the_singleton(B, S, seed):
+    D = 3072
+    dev = _device_inputs(B, S, D, seed)
+    batch = run_step(dev)
+    for b in range(B):
+        _compare_rows(batch, run_step(_one(dev, b)), b, f"B={B} S={S} seed={seed}")
+    # the weight gradient of the batch equals the samples accumulated one by one
+    N = 2 * D
+    accW = torch.empty((N, D), device="cuda")
+    accb = torch.empty((N,), device="cuda")
+    for b in range(B):
+        binding.adaln_proj_bwd(batch["d_emb"][b:b + 1], dev["temb"][b:b + 1], batch["u"][b:b + 1], dev["W"],
+                               dW_acc=accW, db_acc=accb, accumulate=b > 0)
+    dW = torch.empty((N, D), dtype=torch.bfloat16, device="cuda")
+    db = torch.empty((N,), dtype=torch.bfloat16, device="cuda")
+    binding.adaln_proj_bwd(torch.zeros((0, N), device="cuda"), dev["temb"][:0], batch["u"][:0], dev["W"],
+                           dW_acc=accW, db_acc=accb, dW=dW, db=db, accumulate=True)
+    assert torch.equal(_bits(dW), _bits(batch["dW"]))
+    assert torch.equal(_bits(db), _bits(batch["db"]))
+
+
+def test_rows_of_a_2048_batch_match_the_singleton():
+    B, S, D = 2048, 33, 3072
+    dev = _device_inputs(B, S, D, seed=5)
+    batch = run_step(dev)
+    for b in [0, 1, 2, 777, 1023, 1024, 2046, 2047]:
+        _compare_rows(batch, run_step(_one(dev, b)), b, "B=2048")
+
+
+@pytest.mark.parametrize("S", [4096, 6032, 6889])
+def test_two_samples_match_one(S):
+    D = 3072
+    dev = _device_inputs(2, S, D, seed=1, outlier_frac=0.01)
+    batch = run_step(dev)
+    for b in range(2):
+        _compare_rows(batch, run_step(_one(dev, b)), b, f"B=2 vs 1, S={S}")
+
+
+def test_run_to_run_determinism():
+    dev = _device_inputs(2, 4096, 3072, seed=2, outlier_frac=0.01)
+    r1 = run_step(dev)
+    r2 = run_step(dev)
+    for k in r1:
+        assert torch.equal(r1[k].view(torch.uint8), r2[k].view(torch.uint8)), k
+
+
+def _chunked(dev, chunk, D):
+    """Runs the workload in chunks of `chunk` samples; returns per-sample
+    outputs concatenated and dW/db accumulated over the chunks."""
+    n = dev["x"].shape[0]
+    N = 2 * D
+    accW = torch.empty((N, D), device="cuda")
+    accb = torch.empty((N,), device="cuda")
+    outs = {k: [] for k in PER_SAMPLE}
+    for i in range(0, n, chunk):
+        part = {k: (v if k in ("W", "b") else v[i:i + chunk]) for k, v in dev.items()}
+        emb, u = binding.adaln_proj_fwd(part["temb"], part["W"], part["b"])
+        out, mean, rstd = binding.adaln_out_fwd(part["x"], emb)
+        dx, d_emb = binding.adaln_out_bwd(part["dy"], part["x"], emb, mean, rstd)
+        d_temb, _, _, _, _ = binding.adaln_proj_bwd(d_emb, part["temb"], u, part["W"], dW_acc=accW, db_acc=accb,
+                                                    accumulate=i > 0)
+        for k, v in zip(PER_SAMPLE, (emb, u, out, mean, rstd, dx, d_emb, d_temb)):
+            outs[k].append(v)
+    return {k: torch.cat(v) for k, v in outs.items()}, accW, accb
+
+
+@pytest.mark.parametrize("n,chunks", [(256, [256, 128, 16, 4, 1])])
+def test_chunking_invariance(n, chunks):
+    """The chunking workload (samples of S=256) at 256 samples, in five
+    chunkings: every output and dW/db byte-identical."""
+    D, S = 3072, 256
+    dev = _device_inputs(n, S, D, seed=4)
+    ref, refW, refb = _chunked(dev, chunks[0], D)
+    for c in chunks[1:]:
+        got, gW, gb = _chunked(dev, c, D)
+        for k in PER_SAMPLE:
+            assert torch.equal(got[k].view(torch.uint8), ref[k].view(torch.uint8)), (c, k)
+        assert torch.equal(gW.view(torch.int32), refW.view(torch.int32)), c
+        assert torch.equal(gb.view(torch.int32), refb.view(torch.int32)), c
+
+
+@pytest.mark.slow
+def test_chunking_invariance_full_workload():
+    """4096 samples of S=256 as 1x4096, 2x2048, 16x256, 64x64 and 4096x1."""
+    D, S, n = 3072, 256, 4096
+    dev = _device_inputs(n, S, D, seed=6)
+    ref, refW, refb = _chunked(dev, 4096, D)
+    for c in [2048, 256, 64, 1]:
+        got, gW, gb = _chunked(dev, c, D)
+        for k in PER_SAMPLE:
+            assert torch.equal(got[k].view(torch.uint8), ref[k].view(torch.uint8)), (c, k)
+        assert torch.equal(gW.view(torch.int32), refW.view(torch.int32)), c
+        assert torch.equal(gb.view(torch.int32), refb.view(torch.int32)), c
+        del got
