@@ -187,14 +187,13 @@ adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adal
  * start-up.
  *
  * Same arguments, checks, kernels and results (bit for bit) as
- * adaln_out_bwd, without the workspace: the token-tree partials live in a
- * 24 MiB array inside the library, held on every GPU that loads the library
- * until the process exits.  The call allocates nothing.
+ * adaln_out_bwd, without the workspace: what adaln_out_bwd keeps in its
+ * workspace lives in a 24 MiB array inside the library, held on every GPU
+ * that loads the library until the process exits.  The call allocates nothing.
  *
- *   Limit: adaln_out_bwd_workspace_bytes(B, S, D) <= 24 MiB, i.e.
- *   B * ceil(S/32) * 2D * 8 bytes <= 25165824 (at D = 3072: B * ceil(S/32)
- *   <= 512, e.g. B = 2 with S <= 8192).  Larger sizes return ADALN_ERR_SHAPE
- *   before anything is launched.
+ *   Limit: adaln_out_bwd_workspace_bytes(B, S, D) <= 24 MiB = 25165824 bytes
+ *   (at D = 3072: B = 2 with S <= 8192, or B = 1 with S <= 16384).  Larger
+ *   sizes return ADALN_ERR_SHAPE before anything is launched.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -139,6 +139,20 @@ __device__ __forceinline__ void twosum2(float2 &s, float2 &c, float2 v) {
     s = t;
 }
 
+// The Neumaier step itself on two lanes of work: the operand of larger
+// magnitude (|s| >= |v| keeps s) minus t, plus the other operand, is the exact
+// error of t.  Four packed fp32 operations and six selects against TwoSum's
+// seven packed operations: the two forms trade the FMA pipe for the integer
+// pipe, with the same bits.
+__device__ __forceinline__ void neumaier2(float2 &s, float2 &c, float2 v) {
+    const float2 t = f2add(s, v);
+    const bool kx = fabsf(s.x) >= fabsf(v.x), ky = fabsf(s.y) >= fabsf(v.y);
+    const float2 big = make_float2(kx ? s.x : v.x, ky ? s.y : v.y);
+    const float2 small = make_float2(kx ? v.x : s.x, ky ? v.y : s.y);
+    c = f2add(c, f2add(f2sub(big, t), small));
+    s = t;
+}
+
 // --------------------------------------------------------------------------
 // warp reductions with a fixed butterfly; every lane ends with the same bits
 // (each pairwise add is commutative, so partners compute identical values).

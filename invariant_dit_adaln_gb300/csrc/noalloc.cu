@@ -19,8 +19,8 @@
 
 namespace adaln {
 
-// 24 MiB: the level-0 partials of B * ceil(S/32) <= 512 sample-tiles at D = 3072
-// (for instance B = 2 and S <= 8192, or B = 1 and S <= 16384).
+// 24 MiB: the workspace of adaln_out_bwd (the level-0 token-tree partials)
+// for B = 2 and S <= 8192, or B = 1 and S <= 16384, at D = 3072.
 constexpr size_t kNoAllocScratchBytes = 24u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

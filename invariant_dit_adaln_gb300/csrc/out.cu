@@ -287,20 +287,25 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
         for (int s = 0; s < NS; ++s) mbar_init(&my_full[s], 1);
         fence_barrier_init();
     }
-    // warm L2 with the first rows of the ring while the preceding kernel finishes
-    if (lane < NS && lane < nrows) bulk_prefetch_l2(x + (row0 + (size_t)lane * NW) * D, row_bytes);
     __syncwarp();
     pdl_wait();  // x and emb may come from preceding kernels
+    // the sample's modulation parameters are requested before the row copies,
+    // so that they do not queue behind them
+    const uint16_t *e = emb + (size_t)b * 2 * D;
+    uint4 sc0 = make_uint4(0u, 0u, 0u, 0u), sh0 = sc0;
+    if ((int)threadIdx.x < V) {
+        sc0 = ldg16(e + (size_t)threadIdx.x * 8);
+        sh0 = ldg16(e + D + (size_t)threadIdx.x * 8);
+    }
     if (lane == 0)
         for (int k = 0; k < NS && k < nrows; ++k) {
             mbar_arrive_expect_tx(&my_full[k], row_bytes);
             bulk_g2s(my_ring + (size_t)k * row_bytes, x + (row0 + (size_t)k * NW) * D, row_bytes, &my_full[k]);
         }
     // the sample's modulation parameters, fp32
-    const uint16_t *e = emb + (size_t)b * 2 * D;
     for (int i = threadIdx.x; i < V; i += blockDim.x) {
-        const uint4 sc = ldg16(e + (size_t)i * 8);
-        const uint4 sh = ldg16(e + D + (size_t)i * 8);
+        const uint4 sc = i == (int)threadIdx.x ? sc0 : ldg16(e + (size_t)i * 8);
+        const uint4 sh = i == (int)threadIdx.x ? sh0 : ldg16(e + D + (size_t)i * 8);
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
         const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
         float on[8], sf[8];
@@ -527,16 +532,24 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         for (int s = 0; s < NST; ++s) mbar_init(&sm.full[s], 1);
         fence_barrier_init();
     }
-    // warm L2 with the first rows of the ring while the preceding kernel finishes
-    // (only those: the whole tile, for every CTA at once, would not stay in L2)
-    if (tid < min(n, NST)) {
-        bulk_prefetch_l2(x + (row0 + tid) * D, row_bytes);
-        bulk_prefetch_l2(dy + (row0 + tid) * D, row_bytes);
-    }
     __syncthreads();
     pdl_wait();  // mean, rstd, emb (and perhaps x, dy) come from preceding kernels
     pdl_trigger();
 
+    // the row statistics and the sample's scale are requested before the row
+    // copies, so that they do not queue behind them
+    float mu_t = 0.0f, rs_t = 0.0f;
+    if (tid < n) {
+        mu_t = mean[row0 + tid];
+        rs_t = rstd[row0 + tid];
+    }
+    const uint16_t *e = emb + (size_t)b * 2 * D;
+    uint4 sc_v[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + NT * j;
+        sc_v[j] = v < V ? ldg16(e + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
     if (tid == 0) {
         for (int i = 0; i < NST && i < n; ++i) {
             unsigned char *dst = stages + (size_t)i * stage_bytes;
@@ -546,16 +559,15 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         }
     }
     if (tid < n) {
-        sm.mu[tid] = mean[row0 + tid];
-        sm.rs[tid] = rstd[row0 + tid];
+        sm.mu[tid] = mu_t;
+        sm.rs[tid] = rs_t;
     }
     float2 onep[VPT][4];
-    const uint16_t *e = emb + (size_t)b * 2 * D;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
         if (v < V) {
-            const uint4 sc = ldg16(e + (size_t)v * 8);
+            const uint4 sc = sc_v[j];
             const uint32_t w[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

@@ -170,6 +170,11 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
     const int nrows = gw < N ? (N - 1 - gw) / NW + 1 : 0;  // rows of this warp
 
     pdl_wait();  // temb, W, bias may come from preceding kernels
+    // the bias of this warp's rows (lane k holding row k, raw bits) and this
+    // thread's first temb vector are requested before the W rows, so that they
+    // do not queue behind them
+    const uint16_t bias_raw = lane < nrows ? bias[gw + lane * NW] : (uint16_t)0;
+    const uint4 t0 = (int)threadIdx.x < B * V ? ldg16(temb + (size_t)threadIdx.x * 8) : make_uint4(0u, 0u, 0u, 0u);
     uint4 wa[kStreamVL], wb[kStreamVL];
     auto load_row = [&](uint4(&w)[kStreamVL], int n) {
 #pragma unroll
@@ -180,12 +185,10 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
     };
     constexpr int R = BC <= 2 ? 2 : 1;  // rows in flight per warp (registers)
     if (nrows > 0) load_row(wa, gw);
-    // the bias of this warp's rows, lane k holding row k (raw bits: converted at use)
-    const uint16_t bias_raw = lane < nrows ? bias[gw + lane * NW] : (uint16_t)0;
 
     // u = bf16(silu(temb)) for every sample; this CTA stores vectors i = blockIdx.x (mod gridDim.x)
     for (int i = threadIdx.x; i < B * V; i += blockDim.x) {
-        const uint4 t = ldg16(temb + (size_t)i * 8);
+        const uint4 t = i == (int)threadIdx.x ? t0 : ldg16(temb + (size_t)i * 8);
         const uint32_t o[4] = {silu_word(t.x), silu_word(t.y), silu_word(t.z), silu_word(t.w)};
         float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)i * 8);
         dst[0] = make_float4(bf16lo(o[0]), bf16hi(o[0]), bf16lo(o[1]), bf16hi(o[1]));
@@ -291,12 +294,6 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
     const bool want_db = WITH_W && (db_acc != nullptr || db != nullptr) && kchunk == 0 && lane == 0;
     constexpr int kPre = BC <= 2 ? kPreMax : kPreMax / 2;  // fewer rows in flight where more samples need registers
 
-    // warm L2 with this warp's rows of W (an input of the call) while the preceding kernel finishes
-    if (B > 0 && lane < cnt) {
-        const int kv0 = kchunk * 32;
-        const int nvec = min(32, (D >> 3) - kv0);  // vectors of this k-chunk
-        bulk_prefetch_l2(W + (size_t)(n0 + warp + 8 * lane) * D + kv0 * 8, (uint32_t)nvec * 16);
-    }
     pdl_wait();
 
     for (int b0 = 0; b0 < B || (WITH_W && b0 == 0); b0 += BC) {

@@ -55,6 +55,7 @@ def test_status_strings(L):
 
 def test_workspace_sizes(L):
     D = 3072
+    # tree partials (sum, correction) per 32-token tile
     assert L.adaln_out_bwd_workspace_bytes(2, 4096, D) == 2 * 2 * 128 * 6144 * 4
     assert L.adaln_out_bwd_workspace_bytes(2, 33, D) == 2 * 2 * 2 * 6144 * 4
     assert L.adaln_out_bwd_workspace_bytes(0, 33, D) == 0
