@@ -316,12 +316,14 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
             sf[2 * q] = bf16lo(shw[q]);
             sf[2 * q + 1] = bf16hi(shw[q]);
         }
-        float4 *po = reinterpret_cast<float4 *>(t_onep + (size_t)i * 8);
-        float4 *ps = reinterpret_cast<float4 *>(t_shift + (size_t)i * 8);
-        po[0] = make_float4(on[0], on[1], on[2], on[3]);
-        po[1] = make_float4(on[4], on[5], on[6], on[7]);
-        ps[0] = make_float4(sf[0], sf[1], sf[2], sf[3]);
-        ps[1] = make_float4(sf[4], sf[5], sf[6], sf[7]);
+        // two planes of float4 (columns 0-3, then 4-7 of every vector), so that
+        // the lanes of a warp read consecutive 16-byte words
+        float4 *po = reinterpret_cast<float4 *>(t_onep);
+        float4 *ps = reinterpret_cast<float4 *>(t_shift);
+        po[i] = make_float4(on[0], on[1], on[2], on[3]);
+        po[V + i] = make_float4(on[4], on[5], on[6], on[7]);
+        ps[i] = make_float4(sf[0], sf[1], sf[2], sf[3]);
+        ps[V + i] = make_float4(sf[4], sf[5], sf[6], sf[7]);
     }
     __syncthreads();
     pdl_trigger();
@@ -388,9 +390,9 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
         for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
             if (v < V) {
-                const float4 *po = reinterpret_cast<const float4 *>(t_onep + (size_t)v * 8);
-                const float4 *ps = reinterpret_cast<const float4 *>(t_shift + (size_t)v * 8);
-                const float4 oa = po[0], ob = po[1], sa = ps[0], sb = ps[1];
+                const float4 *po = reinterpret_cast<const float4 *>(t_onep);
+                const float4 *ps = reinterpret_cast<const float4 *>(t_shift);
+                const float4 oa = po[v], ob = po[V + v], sa = ps[v], sb = ps[V + v];
                 const float2 onp[4] = {make_float2(oa.x, oa.y), make_float2(oa.z, oa.w), make_float2(ob.x, ob.y),
                                        make_float2(ob.z, ob.w)};
                 const float2 shf[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w), make_float2(sb.x, sb.y),

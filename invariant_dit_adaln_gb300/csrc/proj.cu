@@ -190,9 +190,12 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
     for (int i = threadIdx.x; i < B * V; i += blockDim.x) {
         const uint4 t = i == (int)threadIdx.x ? t0 : ldg16(temb + (size_t)i * 8);
         const uint32_t o[4] = {silu_word(t.x), silu_word(t.y), silu_word(t.z), silu_word(t.w)};
-        float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)i * 8);
-        dst[0] = make_float4(bf16lo(o[0]), bf16hi(o[0]), bf16lo(o[1]), bf16hi(o[1]));
-        dst[1] = make_float4(bf16lo(o[2]), bf16hi(o[2]), bf16lo(o[3]), bf16hi(o[3]));
+        // per sample, two planes of float4 (columns 0-3, then 4-7 of every
+        // vector), so that the lanes of a warp read consecutive 16-byte words
+        const int bi = i / V, vi = i - bi * V;
+        float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)bi * D);
+        dst[vi] = make_float4(bf16lo(o[0]), bf16hi(o[0]), bf16lo(o[1]), bf16hi(o[1]));
+        dst[V + vi] = make_float4(bf16lo(o[2]), bf16hi(o[2]), bf16lo(o[3]), bf16hi(o[3]));
         if (i % gridDim.x == blockIdx.x) stg16(u + (size_t)i * 8, make_uint4(o[0], o[1], o[2], o[3]));
     }
     if (R == 2 && nrows > 1) load_row(wb, gw + NW);
@@ -209,8 +212,8 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
 #pragma unroll
                 for (int b = 0; b < BC; ++b) {
                     if (b < B) {
-                        const float4 *up = reinterpret_cast<const float4 *>(uf + (size_t)b * D + (size_t)v * 8);
-                        const float4 ua = up[0], ub = up[1];
+                        const float4 *up = reinterpret_cast<const float4 *>(uf + (size_t)b * D);
+                        const float4 ua = up[v], ub = up[V + v];
                         acc[b] = dot_pairs(w[j], make_float2(ua.x, ua.y), make_float2(ua.z, ua.w),
                                            make_float2(ub.x, ub.y), make_float2(ub.z, ub.w), acc[b]);
                     }
