@@ -37,6 +37,10 @@ WORKLOAD = dict(B=2, S=4096, D=3072, seed=0, outlier_frac=0.01)
 NOMINAL_HBM_GBS = 8000.0
 FLUSH_BYTES = 512 << 20
 KERNELS_PER_STEP = 6  # SiLU+projection, out_fwd, bwd tile, tree fold, proj-bwd slab, d_temb
+# DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold) at this
+# workload, from the ncu capture summarised in profiles/out_bwd_B2_S4096_D3072.md.  The
+# counters of a replayed launch miss the dx lines still in L2 when it ends.
+OUT_BWD_DRAM_BYTES = 133_250_000
 
 
 # ---------------------------------------------------------------------------
@@ -378,7 +382,7 @@ def run_gpu(args, world, rank, local):
         "calls_ms": call_ms,
         "roofline": {"bound": "hbm", "kernel": dom + " (LN-backward tile kernel + tree fold)",
                      "achieved": ach, "peak": peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                     "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                     "unit": "GB/s", "frac": ach / peak, "traffic": OUT_BWD_DRAM_BYTES,
                      "algorithmic_bytes": cb[dom]},
         "step_roofline": {"achieved": gbs, "peak": peak, "frac": gbs / peak, "unit": "GB/s"},
         "e2e": {"value": throughput(tokens * K3, world, e2e_max), "unit": "tokens/s",

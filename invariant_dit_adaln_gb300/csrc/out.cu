@@ -491,10 +491,10 @@ cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out
 // accumulators (the tile's level-0 node), and each warp publishes its partial
 // sums of gh and gh * x_hat (column pairs in packed fp32x2, the two halves, a
 // fixed butterfly).  After one barrier, one thread per row adds the warps'
-// partials in ascending warp order, giving c1 and c2.  Phase 2 recomputes
-// x_hat and gh from the staged rows (the same operations, so the same bits)
-// and writes dx = rstd * (gh - c1 - x_hat * c2).  The reduction order over d
-// depends on D only.
+// partials in ascending warp order, giving c1 and c2.  Phase 2 recomputes gh
+// and x - mean from the staged rows and writes dx = rstd * (gh - c1 - x_hat *
+// c2), evaluated as rstd gh - rstd c1 + (mean - x) rstd^2 c2 with two fused
+// multiply-adds per column pair.  The reduction order over d depends on D only.
 // ==========================================================================
 constexpr int kRowBlock = 4;    // most rows per block (a block of RB rows, NST = 2 RB stages:
                                 // two blocks of rows in flight)
@@ -627,7 +627,10 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                         a2 = f2fma(gh, xh, a2);
                         // the token product g * x_hat is rounded before it enters the tree
                         const float2 ps = make_float2(__fmul_rn(g2.x, xh.x), __fmul_rn(g2.y, xh.y));
-                        twosum2(sg_s[j][q], kp_s[j][q], ps);
+                        // scalar TwoSum for the scale tree (its products are scalar already):
+                        // the scalar ops can use both FMA pipes, the packed ones only one
+                        twosum(sg_s[j][q].x, kp_s[j][q].x, ps.x);
+                        twosum(sg_s[j][q].y, kp_s[j][q].y, ps.y);
                         twosum2(sg_h[j][q], kp_h[j][q], g2);
                     }
                 }
@@ -648,7 +651,10 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         if (tid < nb) {
             float2 c = sm.red[tid][0];
             for (int w = 1; w < nwarps; ++w) c = f2add(c, sm.red[tid][w]);
-            sm.tot[tid] = make_float2(__fdiv_rn(c.x, Df), __fdiv_rn(c.y, Df));
+            // dx = rstd (gh - c1 - x_hat c2) = rstd gh - rstd c1 + (mean - x) rstd^2 c2
+            const float rsv = sm.rs[r0 + tid];
+            const float c1 = __fdiv_rn(c.x, Df), c2 = __fdiv_rn(c.y, Df);
+            sm.tot[tid] = make_float2(__fmul_rn(rsv, c1), __fmul_rn(__fmul_rn(rsv, rsv), c2));
         }
         __syncthreads();
         // ---- phase 2: dx ----
@@ -659,7 +665,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             const unsigned char *gs = xs + row_bytes;
             const float2 mu2 = f2splat(sm.mu[i]), rs2 = f2splat(sm.rs[i]);
             const float2 c = sm.tot[jr];
-            const float2 nc1 = f2splat(-c.x), nc2 = f2splat(-c.y);
+            const float2 na = f2splat(-c.x), c2r = f2splat(c.y);
             uint16_t *drow = dx + (row0 + i) * D;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
@@ -672,9 +678,9 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                     uint32_t o[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float2 xh = f2mul(f2sub(bf16x2_to_f2(xa[q]), mu2), rs2);
+                        const float2 xm = f2sub(mu2, bf16x2_to_f2(xa[q]));
                         const float2 gh = f2mul(bf16x2_to_f2(ga[q]), onep[j][q]);
-                        const float2 d = f2mul(f2fma(xh, nc2, f2add(gh, nc1)), rs2);
+                        const float2 d = f2fma(xm, c2r, f2fma(rs2, gh, na));
                         o[q] = pack_bf16x2(d.x, d.y);
                     }
                     stg16(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
