@@ -276,13 +276,21 @@ struct SlabSmem {
     float red[8][BC][kProjKChunk];
 };
 
-template <int BC, bool WITH_W>
+// What the slab kernel writes besides the d_silu partials (a template
+// argument, so the per-row loop carries no runtime branches):
+//   kSlabDsOnly   nothing (dW and db come from the tiled kernels)
+//   kSlabDwOut    dW and db in bf16, overwrite, no fp32 accumulators
+//   kSlabGeneral  any of dW_acc, db_acc (accumulate or overwrite), dW, db
+constexpr int kSlabDsOnly = 0, kSlabDwOut = 1, kSlabGeneral = 2;
+
+template <int BC, int WM>
 __global__ void __launch_bounds__(256, 2)
 proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, const uint16_t *__restrict__ W,
                      float *__restrict__ dW_acc, float *__restrict__ db_acc, uint16_t *__restrict__ dW,
                      uint16_t *__restrict__ db, int accumulate, float *__restrict__ ws, int B, int D) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     SlabSmem<BC> &sm = *reinterpret_cast<SlabSmem<BC> *>(smem_raw);
+    constexpr bool WITH_W = WM != kSlabDsOnly;
     const int kchunk = blockIdx.x;
     const int slab = blockIdx.y;
     const int warp = threadIdx.x >> 5;
@@ -293,8 +301,9 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
     const bool live_k = kv < (D >> 3);
     const int col = kv * 8;
     const int cnt = min(kRowsPerWarp, (N - n0) / 8);  // rows per warp, equal for all warps (N % 16 == 0)
-    const bool want_dw = WITH_W && (dW_acc != nullptr || dW != nullptr);
-    const bool want_db = WITH_W && (db_acc != nullptr || db != nullptr) && kchunk == 0 && lane == 0;
+    const bool want_dw = WM == kSlabDwOut || (WM == kSlabGeneral && (dW_acc != nullptr || dW != nullptr));
+    const bool want_db = (WM == kSlabDwOut || (WM == kSlabGeneral && (db_acc != nullptr || db != nullptr))) &&
+                         kchunk == 0 && lane == 0;
     constexpr int kPre = BC <= 2 ? kPreMax : kPreMax / 2;  // fewer rows in flight where more samples need registers
 
     pdl_wait();
@@ -306,23 +315,22 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
             const int n = n0 + r;
             sm.es[b][r] = (b < nb && n < N) ? bf16f(bf16_bits(d_emb[(size_t)(b0 + b) * N + n])) : 0.0f;
         }
-        float uf[BC][8];
+        float2 uf[BC][4];  // u of this lane's 8 columns, by column pair
 #pragma unroll
         for (int b = 0; b < BC; ++b) {
-            if (WITH_W && b < nb && live_k) {
-                unpack8(ldg16(u + (size_t)(b0 + b) * D + col), uf[b]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) uf[b][q] = 0.0f;
-            }
+            const uint4 uv = (WITH_W && b < nb && live_k) ? ldg16(u + (size_t)(b0 + b) * D + col) : make_uint4(0u, 0u, 0u, 0u);
+            uf[b][0] = bf16x2_to_f2(uv.x); uf[b][1] = bf16x2_to_f2(uv.y);
+            uf[b][2] = bf16x2_to_f2(uv.z); uf[b][3] = bf16x2_to_f2(uv.w);
         }
         __syncthreads();
 
-        float ds[BC][8];
+        // d_silu partials of this lane's columns, by column pair (each lane of a
+        // packed operation is one column, in its own sequential order)
+        float2 ds[BC][4];
 #pragma unroll
         for (int b = 0; b < BC; ++b)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) ds[b][q] = 0.0f;
+            for (int q = 0; q < 4; ++q) ds[b][q] = make_float2(0.0f, 0.0f);
 
         for (int i0 = 0; i0 < cnt; i0 += kPre) {
             uint4 wv[kPre];
@@ -338,58 +346,63 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                 if (i < cnt && live_k) {
                     const int r = warp + 8 * i;
                     const int n = n0 + r;
-                    float w[8];
-                    unpack8(wv[p], w);
+                    const float2 w2[4] = {bf16x2_to_f2(wv[p].x), bf16x2_to_f2(wv[p].y), bf16x2_to_f2(wv[p].z),
+                                          bf16x2_to_f2(wv[p].w)};
+                    float2 e2[BC];
 #pragma unroll
-                    for (int b = 0; b < BC; ++b) {
+                    for (int b = 0; b < BC; ++b) e2[b] = f2splat(sm.es[b][r]);
+#pragma unroll
+                    for (int b = 0; b < BC; ++b)
                         if (b < nb) {
-                            const float e = sm.es[b][r];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) ds[b][q] = __fmaf_rn(e, w[q], ds[b][q]);
+                            for (int q = 0; q < 4; ++q) ds[b][q] = f2fma(e2[b], w2[q], ds[b][q]);
                         }
-                    }
-                    if (want_dw) {
-                        float acc[8];
-                        float *pa = dW_acc ? dW_acc + (size_t)n * D + col : nullptr;
-                        if (accumulate) {
+                    if (WITH_W && want_dw) {
+                        // acc = (accumulate ? acc_in : +0), then + e[b,n] * u[b,k] for b ascending
+                        float2 acc[4];
+                        float *pa = (WM == kSlabGeneral && dW_acc) ? dW_acc + (size_t)n * D + col : nullptr;
+                        if (WM == kSlabGeneral && accumulate) {
                             const float4 a0 = *reinterpret_cast<const float4 *>(pa);
                             const float4 a1 = *reinterpret_cast<const float4 *>(pa + 4);
-                            acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
-                            acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+                            acc[0] = make_float2(a0.x, a0.y); acc[1] = make_float2(a0.z, a0.w);
+                            acc[2] = make_float2(a1.x, a1.y); acc[3] = make_float2(a1.z, a1.w);
                         } else {
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                            for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.0f, 0.0f);
                         }
 #pragma unroll
-                        for (int b = 0; b < BC; ++b) {
+                        for (int b = 0; b < BC; ++b)
                             if (b < nb) {
-                                const float e = sm.es[b][r];
 #pragma unroll
-                                for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(e, uf[b][q], acc[q]);
+                                for (int q = 0; q < 4; ++q) acc[q] = f2fma(e2[b], uf[b][q], acc[q]);
                             }
+                        if (WM == kSlabGeneral && pa) {
+                            stg16f(pa, make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y));
+                            stg16f(pa + 4, make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y));
                         }
-                        if (pa) {
-                            stg16f(pa, make_float4(acc[0], acc[1], acc[2], acc[3]));
-                            stg16f(pa + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
-                        }
-                        if (dW) stg16(dW + (size_t)n * D + col, pack8(acc));
+                        if (WM == kSlabDwOut || dW)
+                            stg16(dW + (size_t)n * D + col,
+                                  make_uint4(pack_bf16x2(acc[0].x, acc[0].y), pack_bf16x2(acc[1].x, acc[1].y),
+                                             pack_bf16x2(acc[2].x, acc[2].y), pack_bf16x2(acc[3].x, acc[3].y)));
                     }
                 }
-                if (want_db && i < cnt) {
+                if (WITH_W && want_db && i < cnt) {
                     const int r = warp + 8 * i;
                     const int n = n0 + r;
-                    float a = accumulate ? db_acc[n] : 0.0f;
+                    float a = (WM == kSlabGeneral && accumulate) ? db_acc[n] : 0.0f;
                     for (int b = 0; b < nb; ++b) a = __fadd_rn(a, sm.es[b][r]);
-                    if (db_acc) db_acc[n] = a;
-                    if (db) db[n] = bf16_bits(a);
+                    if (WM == kSlabGeneral && db_acc) db_acc[n] = a;
+                    if (WM == kSlabDwOut || db) db[n] = bf16_bits(a);
                 }
             }
         }
         // the slab's partial d_silu: warps added in ascending order
 #pragma unroll
-        for (int b = 0; b < BC; ++b)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sm.red[warp][b][lane * 8 + q] = ds[b][q];
+        for (int b = 0; b < BC; ++b) {
+            float4 *dst = reinterpret_cast<float4 *>(&sm.red[warp][b][lane * 8]);
+            dst[0] = make_float4(ds[b][0].x, ds[b][0].y, ds[b][1].x, ds[b][1].y);
+            dst[1] = make_float4(ds[b][2].x, ds[b][2].y, ds[b][3].x, ds[b][3].y);
+        }
         __syncthreads();
         for (int i = threadIdx.x; i < nb * kProjKChunk; i += blockDim.x) {
             const int b = i / kProjKChunk, c = i % kProjKChunk;
@@ -589,18 +602,28 @@ int read_and_clear_proj_error() {
     return (int)v;
 }
 
-template <int BC, bool WITH_W>
+template <int BC, int WM>
 static cudaError_t launch_slab(const float *d_emb, const uint16_t *u, const uint16_t *W, float *dW_acc, float *db_acc,
                                uint16_t *dW, uint16_t *db, int accumulate, float *ws, int B, int D,
                                cudaStream_t stream, const DeviceInfo &dev) {
     const size_t smem = sizeof(SlabSmem<BC>);
-    auto kern = proj_bwd_slab_kernel<BC, WITH_W>;
+    auto kern = proj_bwd_slab_kernel<BC, WM>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     const int nslab = (2 * D + kSlabRows - 1) / kSlabRows;
     const int nk = (D + kProjKChunk - 1) / kProjKChunk;
     return launch_pdl(kern, dim3(nk, nslab), dim3(256), smem, stream, d_emb, u, W, dW_acc, db_acc, dW, db,
                       accumulate, ws, B, D);
+}
+
+template <int BC>
+static cudaError_t launch_slab_w(const float *d_emb, const uint16_t *u, const uint16_t *W, float *dW_acc,
+                                 float *db_acc, uint16_t *dW, uint16_t *db, int accumulate, float *ws, int B, int D,
+                                 cudaStream_t stream, const DeviceInfo &dev) {
+    // dW and db both wanted in bf16, nothing accumulated: the branch-free form
+    if (!dW_acc && !db_acc && !accumulate && dW && db)
+        return launch_slab<BC, kSlabDwOut>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+    return launch_slab<BC, kSlabGeneral>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
 }
 
 cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
@@ -612,11 +635,11 @@ cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint
     cudaError_t err;
     if (B <= 4) {
         // one pass over W: d_silu partials and (when asked) dW / db
-        if (B <= 1) err = launch_slab<1, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
-        else if (B == 2) err = launch_slab<2, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
-        else err = launch_slab<4, true>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+        if (B <= 1) err = launch_slab_w<1>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+        else if (B == 2) err = launch_slab_w<2>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+        else err = launch_slab_w<4>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
     } else {
-        err = launch_slab<4, false>(d_emb, u, W, nullptr, nullptr, nullptr, nullptr, 0, ws, B, D, stream, dev);
+        err = launch_slab<4, kSlabDsOnly>(d_emb, u, W, nullptr, nullptr, nullptr, nullptr, 0, ws, B, D, stream, dev);
         if (err == cudaSuccess && (dW_acc || dW))
             err = launch_pdl(proj_dw_tiled_kernel, dim3((D + kDwTile - 1) / kDwTile, (N + kDwTile - 1) / kDwTile),
                              dim3(256), 0, stream, d_emb, u, dW_acc, dW, accumulate, B, D);
