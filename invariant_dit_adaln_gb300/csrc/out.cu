@@ -771,28 +771,41 @@ struct FoldSmem {
 
 // one group of the fold: Neumaier sum of the children's sums in ascending
 // order (compensation c), children's corrections added in ascending order;
-// node = (sum, c + corrections).  Children are loaded eight at a time.
+// node = (sum, c + corrections).  Children are loaded eight at a time, the next
+// eight in flight while the current ones are added.
+__device__ __forceinline__ void fold_load8(const float *sig, const float *kap, size_t stride, int i0, int count,
+                                           float (&vs)[8], float (&vk)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (i0 + q < count) {
+            vs[q] = sig[(size_t)(i0 + q) * stride];
+            vk[q] = kap[(size_t)(i0 + q) * stride];
+        }
+}
+__device__ __forceinline__ void fold_add8(const float (&vs)[8], const float (&vk)[8], int i0, int count, float &s,
+                                          float &c, float &k) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        if (i0 + q == 0) {
+            s = vs[0];
+            k = vk[0];
+        } else if (i0 + q < count) {
+            twosum(s, c, vs[q]);
+            k = __fadd_rn(k, vk[q]);
+        }
+    }
+}
 __device__ __forceinline__ void fold_group(const float *sig, const float *kap, size_t stride, int count,
                                            float &out_s, float &out_k) {
     float s = 0.0f, c = 0.0f, k = 0.0f;
-    for (int i0 = 0; i0 < count; i0 += 8) {
-        float vs[8], vk[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (i0 + q < count) {
-                vs[q] = sig[(size_t)(i0 + q) * stride];
-                vk[q] = kap[(size_t)(i0 + q) * stride];
-            }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (i0 + q == 0) {
-                s = vs[0];
-                k = vk[0];
-            } else if (i0 + q < count) {
-                twosum(s, c, vs[q]);
-                k = __fadd_rn(k, vk[q]);
-            }
-        }
+    float as[8], ak[8], bs[8], bk[8];
+    fold_load8(sig, kap, stride, 0, count, as, ak);
+    if (8 < count) fold_load8(sig, kap, stride, 8, count, bs, bk);
+    for (int i0 = 0; i0 < count; i0 += 16) {
+        fold_add8(as, ak, i0, count, s, c, k);
+        if (i0 + 16 < count) fold_load8(sig, kap, stride, i0 + 16, count, as, ak);
+        if (i0 + 8 < count) fold_add8(bs, bk, i0 + 8, count, s, c, k);
+        if (i0 + 24 < count) fold_load8(sig, kap, stride, i0 + 24, count, bs, bk);
     }
     out_s = s;
     out_k = __fadd_rn(c, k);

@@ -268,7 +268,7 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
 // --------------------------------------------------------------------------
 constexpr int kSlabRows = kProjSlabRows;        // 256
 constexpr int kRowsPerWarp = kSlabRows / 8;     // 32
-constexpr int kPreMax = 16;                      // rows of W in flight per warp (up to 2 samples)
+constexpr int kPreMax = 8;                       // rows of W per register batch (two batches, up to 2 samples)
 
 template <int BC>
 struct SlabSmem {
@@ -332,14 +332,18 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
 #pragma unroll
             for (int q = 0; q < 4; ++q) ds[b][q] = make_float2(0.0f, 0.0f);
 
-        for (int i0 = 0; i0 < cnt; i0 += kPre) {
-            uint4 wv[kPre];
+        // W rows in two register batches of kPre, double-buffered: one batch is
+        // in flight while the other is used
+        uint4 wa[kPre], wb[kPre];
+        auto load_batch = [&](uint4(&wv)[kPre], int i0) {
 #pragma unroll
             for (int p = 0; p < kPre; ++p) {
                 const int n = n0 + warp + 8 * (i0 + p);
                 wv[p] = make_uint4(0u, 0u, 0u, 0u);  // W is not read without samples
                 if (i0 + p < cnt && live_k && nb > 0) wv[p] = ldg16(W + (size_t)n * D + col);
             }
+        };
+        auto use_batch = [&](const uint4(&wv)[kPre], int i0) {
 #pragma unroll
             for (int p = 0; p < kPre; ++p) {
                 const int i = i0 + p;
@@ -395,6 +399,14 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                     if (WM == kSlabDwOut || db) db[n] = bf16_bits(a);
                 }
             }
+        };
+        load_batch(wa, 0);
+        load_batch(wb, kPre);
+        for (int i0 = 0; i0 < cnt; i0 += 2 * kPre) {
+            use_batch(wa, i0);
+            if (i0 + 2 * kPre < cnt) load_batch(wa, i0 + 2 * kPre);
+            use_batch(wb, i0 + kPre);
+            if (i0 + 3 * kPre < cnt) load_batch(wb, i0 + 3 * kPre);
         }
         // the slab's partial d_silu: warps added in ascending order
 #pragma unroll
