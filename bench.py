@@ -36,7 +36,7 @@ METRIC = "AdaLN-out fwd+bwd tokens/s and HBM GB/s (% of 8 TB/s) at B=2,S=4096,D=
 WORKLOAD = dict(B=2, S=4096, D=3072, seed=0, outlier_frac=0.01)
 NOMINAL_HBM_GBS = 8000.0
 FLUSH_BYTES = 512 << 20
-KERNELS_PER_STEP = 6  # SiLU+projection, out_fwd, bwd tile, tree fold, proj-bwd slab, d_temb
+KERNELS_PER_STEP = 7  # SiLU, projection, out_fwd, bwd tile, tree fold, proj-bwd slab, d_temb
 # DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold) at this
 # workload, from the ncu capture summarised in profiles/out_bwd_B2_S4096_D3072.md.  The
 # counters of a replayed launch miss the dx lines still in L2 when it ends.

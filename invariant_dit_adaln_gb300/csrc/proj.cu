@@ -139,14 +139,16 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
 }
 
 // --------------------------------------------------------------------------
-// The same projection for up to kStreamMaxB samples in one kernel, SiLU
-// included.  Every CTA computes u = bf16(silu(temb)) for all samples into
-// shared memory (as fp32; it also writes its share of u), while the first W
-// row of each warp is already in flight: warp gw (global index, NW warps in
-// all) takes rows n = gw, gw + NW, ..., two at a time for up to 2 samples (one
-// otherwise), each lane loading its vectors v = lane + 32 j of the rows into
-// registers (16-byte loads) before any arithmetic.  The order of the terms is the one above, so both kernels
-// give the same bits.
+// The same projection for up to kStreamMaxB samples, after the SiLU kernel.
+// W and bias are inputs of this call, and the kernel before this one is the
+// SiLU kernel, which waits for all earlier work to complete before it lets
+// this one start: the first W rows of every warp and the bias are loaded
+// before this kernel's own wait, and stream in while SiLU runs.  Then u is
+// staged in shared memory (fp32, two float4 planes per sample), and warp gw
+// (global index, NW warps in all) takes rows n = gw, gw + NW, ..., two at a
+// time for up to 2 samples (one otherwise), each lane holding its vectors
+// v = lane + 32 j of the rows in registers.  The order of the terms is the
+// one above, so both kernels give the same bits.
 // --------------------------------------------------------------------------
 constexpr int kStreamMaxB = 8;
 constexpr int kStreamWarps = 8;
@@ -156,9 +158,8 @@ static __device__ unsigned g_proj_err;  // device-side error word of this file's
 
 template <int BC>
 __global__ void __launch_bounds__(kStreamWarps * 32, 2)
-proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__restrict__ W,
-                       const uint16_t *__restrict__ bias, uint16_t *__restrict__ emb, uint16_t *__restrict__ u,
-                       int B, int D) {
+proj_fwd_stream_kernel(const uint16_t *__restrict__ u, const uint16_t *__restrict__ W,
+                       const uint16_t *__restrict__ bias, uint16_t *__restrict__ emb, int B, int D) {
     extern __shared__ __align__(128) float uf[];  // [B][D] fp32
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -169,12 +170,6 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
     const int gw = blockIdx.x * kStreamWarps + warp;
     const int nrows = gw < N ? (N - 1 - gw) / NW + 1 : 0;  // rows of this warp
 
-    pdl_wait();  // temb, W, bias may come from preceding kernels
-    // the bias of this warp's rows (lane k holding row k, raw bits) and this
-    // thread's first temb vector are requested before the W rows, so that they
-    // do not queue behind them
-    const uint16_t bias_raw = lane < nrows ? bias[gw + lane * NW] : (uint16_t)0;
-    const uint4 t0 = (int)threadIdx.x < B * V ? ldg16(temb + (size_t)threadIdx.x * 8) : make_uint4(0u, 0u, 0u, 0u);
     uint4 wa[kStreamVL], wb[kStreamVL];
     auto load_row = [&](uint4(&w)[kStreamVL], int n) {
 #pragma unroll
@@ -184,21 +179,22 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ temb, const uint16_t *__rest
         }
     };
     constexpr int R = BC <= 2 ? 2 : 1;  // rows in flight per warp (registers)
+    // the bias of this warp's rows (lane k holding row k, raw bits), then the first rows of W
+    const uint16_t bias_raw = lane < nrows ? bias[gw + lane * NW] : (uint16_t)0;
     if (nrows > 0) load_row(wa, gw);
+    if (R == 2 && nrows > 1) load_row(wb, gw + NW);
+    pdl_wait();  // u comes from the SiLU kernel
 
-    // u = bf16(silu(temb)) for every sample; this CTA stores vectors i = blockIdx.x (mod gridDim.x)
+    // u of every sample as fp32, per sample two planes of float4 (columns 0-3,
+    // then 4-7 of every vector), so that the lanes of a warp read consecutive
+    // 16-byte words
     for (int i = threadIdx.x; i < B * V; i += blockDim.x) {
-        const uint4 t = i == (int)threadIdx.x ? t0 : ldg16(temb + (size_t)i * 8);
-        const uint32_t o[4] = {silu_word(t.x), silu_word(t.y), silu_word(t.z), silu_word(t.w)};
-        // per sample, two planes of float4 (columns 0-3, then 4-7 of every
-        // vector), so that the lanes of a warp read consecutive 16-byte words
+        const uint4 t = ldg16(u + (size_t)i * 8);
         const int bi = i / V, vi = i - bi * V;
         float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)bi * D);
-        dst[vi] = make_float4(bf16lo(o[0]), bf16hi(o[0]), bf16lo(o[1]), bf16hi(o[1]));
-        dst[V + vi] = make_float4(bf16lo(o[2]), bf16hi(o[2]), bf16lo(o[3]), bf16hi(o[3]));
-        if (i % gridDim.x == blockIdx.x) stg16(u + (size_t)i * 8, make_uint4(o[0], o[1], o[2], o[3]));
+        dst[vi] = make_float4(bf16lo(t.x), bf16hi(t.x), bf16lo(t.y), bf16hi(t.y));
+        dst[V + vi] = make_float4(bf16lo(t.z), bf16hi(t.z), bf16lo(t.w), bf16hi(t.w));
     }
-    if (R == 2 && nrows > 1) load_row(wb, gw + NW);
     __syncthreads();
     pdl_trigger();
 
@@ -552,9 +548,8 @@ static cudaError_t launch_proj_fwd_gemv(const uint16_t *W, const uint16_t *bias,
 }
 
 template <int BC>
-static cudaError_t launch_proj_fwd_stream(const uint16_t *temb, const uint16_t *W, const uint16_t *bias,
-                                          uint16_t *emb, uint16_t *u, int B, int D, size_t smem, cudaStream_t stream,
-                                          const DeviceInfo &dev) {
+static cudaError_t launch_proj_fwd_stream(const uint16_t *u, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
+                                          int B, int D, size_t smem, cudaStream_t stream, const DeviceInfo &dev) {
     auto kern = proj_fwd_stream_kernel<BC>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
@@ -566,7 +561,7 @@ static cudaError_t launch_proj_fwd_stream(const uint16_t *temb, const uint16_t *
     int grid = dev.sm_count * per_sm;
     const int need = (N + kStreamWarps - 1) / kStreamWarps;
     if (grid > need) grid = need;
-    return launch_pdl(kern, dim3(grid), dim3(kStreamWarps * 32), smem, stream, temb, W, bias, emb, u, B, D);
+    return launch_pdl(kern, dim3(grid), dim3(kStreamWarps * 32), smem, stream, u, W, bias, emb, B, D);
 }
 
 // The SiLU table of the current device, filled by its first call: launched on
@@ -586,23 +581,23 @@ static cudaError_t ensure_silu_table(cudaStream_t stream, const DeviceInfo &dev)
     return err;
 }
 
-// Up to kStreamMaxB samples and D <= 3072: the fused kernel; otherwise the
-// SiLU kernel, then the chunked GEMV.
+// The SiLU kernel, then: up to kStreamMaxB samples and D <= 3072, the
+// streaming GEMV; otherwise the chunked GEMV.
 cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
                             uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
     if (B == 0) return cudaSuccess;
-    cudaError_t terr = ensure_silu_table(stream, dev);
-    if (terr != cudaSuccess) return terr;
-    const size_t smem = (size_t)B * D * 4;
-    if (B <= kStreamMaxB && D / 8 <= 32 * kStreamVL) {
-        if (B == 1) return launch_proj_fwd_stream<1>(temb, W, bias, emb, u, B, D, smem, stream, dev);
-        if (B == 2) return launch_proj_fwd_stream<2>(temb, W, bias, emb, u, B, D, smem, stream, dev);
-        if (B <= 4) return launch_proj_fwd_stream<4>(temb, W, bias, emb, u, B, D, smem, stream, dev);
-        return launch_proj_fwd_stream<8>(temb, W, bias, emb, u, B, D, smem, stream, dev);
-    }
-    const long long n8 = (long long)B * D / 8;
-    cudaError_t err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
+    cudaError_t err = ensure_silu_table(stream, dev);
     if (err != cudaSuccess) return err;
+    const long long n8 = (long long)B * D / 8;
+    err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
+    if (err != cudaSuccess) return err;
+    if (B <= kStreamMaxB && D / 8 <= 32 * kStreamVL) {
+        const size_t smem = (size_t)B * D * 4;
+        if (B == 1) return launch_proj_fwd_stream<1>(u, W, bias, emb, B, D, smem, stream, dev);
+        if (B == 2) return launch_proj_fwd_stream<2>(u, W, bias, emb, B, D, smem, stream, dev);
+        if (B <= 4) return launch_proj_fwd_stream<4>(u, W, bias, emb, B, D, smem, stream, dev);
+        return launch_proj_fwd_stream<8>(u, W, bias, emb, B, D, smem, stream, dev);
+    }
     if (B <= 4) return launch_proj_fwd_gemv<4>(W, bias, u, emb, B, D, stream, dev);
     return launch_proj_fwd_gemv<8>(W, bias, u, emb, B, D, stream, dev);
 }
