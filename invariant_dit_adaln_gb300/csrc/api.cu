@@ -264,10 +264,7 @@ adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const ad
 
 int adaln_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    const int a = read_and_clear_device_error();
-    const int b = read_and_clear_proj_error();
-    if (a < 0 || b < 0) return -1;
-    return a != 0 ? a : b;
+    return read_and_clear_device_error();
 }
 
 }  // extern "C"

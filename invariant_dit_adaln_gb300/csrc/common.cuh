@@ -27,7 +27,6 @@ enum DeviceError : unsigned {
     kErrNone = 0,
     kErrOutFwdWait = 0x101,
     kErrOutBwdWait = 0x201,
-    kErrProjWait = 0x301,
 };
 
 // --------------------------------------------------------------------------
@@ -44,22 +43,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
-// unpack 8 bf16 (one 16-byte vector) into floats
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
-    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
-    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint4 v;
-    v.x = pack_bf16x2(f[0], f[1]);
-    v.y = pack_bf16x2(f[2], f[3]);
-    v.z = pack_bf16x2(f[4], f[5]);
-    v.w = pack_bf16x2(f[6], f[7]);
-    return v;
 }
 
 // a packed bf16x2 word as (lo, hi) floats: exact
@@ -136,20 +119,6 @@ __device__ __forceinline__ void twosum2(float2 &s, float2 &c, float2 v) {
     const float2 bp = f2sub(t, s);
     const float2 e = f2add(f2sub(s, f2sub(t, bp)), f2sub(v, bp));
     c = f2add(c, e);
-    s = t;
-}
-
-// The Neumaier step itself on two lanes of work: the operand of larger
-// magnitude (|s| >= |v| keeps s) minus t, plus the other operand, is the exact
-// error of t.  Four packed fp32 operations and six selects against TwoSum's
-// seven packed operations: the two forms trade the FMA pipe for the integer
-// pipe, with the same bits.
-__device__ __forceinline__ void neumaier2(float2 &s, float2 &c, float2 v) {
-    const float2 t = f2add(s, v);
-    const bool kx = fabsf(s.x) >= fabsf(v.x), ky = fabsf(s.y) >= fabsf(v.y);
-    const float2 big = make_float2(kx ? s.x : v.x, ky ? s.y : v.y);
-    const float2 small = make_float2(kx ? v.x : s.x, ky ? v.y : s.y);
-    c = f2add(c, f2add(f2sub(big, t), small));
     s = t;
 }
 

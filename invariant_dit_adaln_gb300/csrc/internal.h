@@ -53,6 +53,5 @@ cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint1
 cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
                             uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
                             int accumulate, void *ws, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
-int read_and_clear_proj_error();
 
 }  // namespace adaln

@@ -154,8 +154,6 @@ constexpr int kStreamMaxB = 8;
 constexpr int kStreamWarps = 8;
 constexpr int kStreamVL = 12;  // W vectors per lane and row held in registers (D <= 3072)
 
-static __device__ unsigned g_proj_err;  // device-side error word of this file's kernels
-
 template <int BC>
 __global__ void __launch_bounds__(kStreamWarps * 32, 2)
 proj_fwd_stream_kernel(const uint16_t *__restrict__ u, const uint16_t *__restrict__ W,
@@ -602,12 +600,6 @@ cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint1
     return launch_proj_fwd_gemv<8>(W, bias, u, emb, B, D, stream, dev);
 }
 
-int read_and_clear_proj_error() {
-    unsigned v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_proj_err, sizeof(v)) != cudaSuccess) return -1;
-    if (v != 0 && cudaMemcpyToSymbol(g_proj_err, &zero, sizeof(zero)) != cudaSuccess) return -1;
-    return (int)v;
-}
 
 template <int BC, int WM>
 static cudaError_t launch_slab(const float *d_emb, const uint16_t *u, const uint16_t *W, float *dW_acc, float *db_acc,
