@@ -221,7 +221,11 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist_mod = init_dist(world, "nccl")
-    build.build()
+    # one rank builds (a no-op when the library is up to date); the others wait
+    # for it rather than compile into the same files at the same time
+    if rank == 0:
+        build.build()
+    barrier(dist_mod, device)
     binding.load()
 
     W_ = WORKLOAD
