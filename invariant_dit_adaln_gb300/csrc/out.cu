@@ -488,9 +488,10 @@ cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out
 // are taken in blocks of kRowBlock rows.  Phase 1, per row in ascending s:
 // x_hat = (x - mean) * rstd (bit-identical to the forward's), g = fp32(dy),
 // gh = g * onep; the row's products g * x_hat and g go into the columns' tree
-// accumulators (the tile's level-0 node), and each warp publishes its partial
-// sums of gh and gh * x_hat (column pairs in packed fp32x2, the two halves, a
-// fixed butterfly).  After one barrier, one thread per row adds the warps'
+// accumulators (the tile's level-0 node), and each thread keeps its partial
+// sums of gh and gh * x_hat (column pairs in packed fp32x2, the two halves);
+// after the block's rows each warp reduces all of them at once (a fixed
+// transposed butterfly) and publishes them.  After one barrier, one thread per row adds the warps'
 // partials in ascending warp order, giving c1 and c2.  Phase 2 recomputes gh
 // and x - mean from the staged rows and writes dx = rstd * (gh - c1 - x_hat *
 // c2), evaluated as rstd gh - rstd c1 + (mean - x) rstd^2 c2 with two fused
@@ -601,6 +602,9 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         const int nb = min(RB, n - r0);
         // ---- phase 1: tree products and the row sums ----
         bool ok = true;
+        float rsum[2 * kRowBlock];  // this thread's (sum gh, sum gh * x_hat) of each row of the block
+#pragma unroll
+        for (int q = 0; q < 2 * kRowBlock; ++q) rsum[q] = 0.0f;
         #pragma unroll
         for (int jr = 0; jr < RB; ++jr) if (jr < nb) {
             const int i = r0 + jr;
@@ -635,8 +639,43 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                     }
                 }
             }
-            const float2 part = warp_sum2(make_float2(__fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y)));
-            if (lane == 0) sm.red[jr][warp] = part;
+            rsum[2 * jr] = __fadd_rn(a1.x, a1.y);
+            rsum[2 * jr + 1] = __fadd_rn(a2.x, a2.y);
+        }
+        {
+            // The block's 2 RB sums over the warp's 32 lanes at once (a transposed
+            // butterfly): at each of the first levels a lane keeps half of its
+            // values and adds the partner's copy of them; after the last level
+            // lane l holds value (l >> 2) summed over all lanes, in a fixed tree.
+            static_assert(RB == 4 || RB == 2, "blocks of 2 or 4 rows");
+            float w4[4], w2[2];
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            if (RB == 4) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float keep = b4 ? rsum[q + 4] : rsum[q], give = b4 ? rsum[q] : rsum[q + 4];
+                    w4[q] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 16));
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w4[q] = __fadd_rn(rsum[q], __shfl_xor_sync(0xFFFFFFFFu, rsum[q], 16));
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float keep = b3 ? w4[q + 2] : w4[q], give = b3 ? w4[q] : w4[q + 2];
+                w2[q] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 8));
+            }
+            const float keep = b2 ? w2[1] : w2[0], give = b2 ? w2[0] : w2[1];
+            float v = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 4));
+            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+            // value index: (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0) = 2 jr + quantity (RB == 4);
+            // with RB == 2 the upper half is never kept and lanes 0-15 hold the values
+            const int idx = (lane >> 2) & 7;
+            if ((lane & 3) == 0 && idx < 2 * RB) {
+                float *dst = reinterpret_cast<float *>(&sm.red[idx >> 1][warp]);
+                dst[idx & 1] = v;
+            }
         }
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
