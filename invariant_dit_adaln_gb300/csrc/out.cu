@@ -596,7 +596,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         for (int q = 0; q < 4; ++q) {
             sg_s[j][q] = kp_s[j][q] = sg_h[j][q] = kp_h[j][q] = make_float2(0.0f, 0.0f);
         }
-    const float Df = (float)D;
+    const float invD = __frcp_rn((float)D);  // c1, c2 only feed dx (tolerance-checked)
 
     for (int r0 = 0; r0 < n; r0 += RB) {
         const int nb = min(RB, n - r0);
@@ -692,7 +692,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             for (int w = 1; w < nwarps; ++w) c = f2add(c, sm.red[tid][w]);
             // dx = rstd (gh - c1 - x_hat c2) = rstd gh - rstd c1 + (mean - x) rstd^2 c2
             const float rsv = sm.rs[r0 + tid];
-            const float c1 = __fdiv_rn(c.x, Df), c2 = __fdiv_rn(c.y, Df);
+            const float c1 = __fmul_rn(c.x, invD), c2 = __fmul_rn(c.y, invD);
             sm.tot[tid] = make_float2(__fmul_rn(rsv, c1), __fmul_rn(__fmul_rn(rsv, rsv), c2));
         }
         __syncthreads();
@@ -727,17 +727,17 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             }
         }
         __syncthreads();  // every thread is done with this block's stages
-        if (tid == 0)
-            for (int jr = 0; jr < nb; ++jr) {
-                const int i = r0 + jr;
-                if (i + NST < n) {
-                    const int st = i % NST;
-                    unsigned char *dst = stages + (size_t)st * stage_bytes;
-                    mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
-                    bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
-                    bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
-                }
+        // lanes 0 .. nb-1 of warp 0 re-arm one stage each (each stage has its own barrier)
+        if (tid < nb) {
+            const int i = r0 + tid;
+            if (i + NST < n) {
+                const int st = i % NST;
+                unsigned char *dst = stages + (size_t)st * stage_bytes;
+                mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
+                bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
             }
+        }
     }
     // level-0 node of this tile: scale half at columns [0, D), shift half at [D, 2D)
     const int H = 2 * D;
