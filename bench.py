@@ -361,55 +361,85 @@ def run_gpu(args, world, rank, local):
     dev_in = {"x": x, "dy": dy, "temb": temb, "W": W, "b": b}
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
-    # Copies in on one stream, in the order the calls need their inputs; copies
-    # out on another, as soon as the call that writes a tensor has finished;
-    # the calls on the compute stream.  The timed region spans all of them.
+    # A stream of steps, each with its own host inputs copied in and its results
+    # copied out, pipelined over two sets of device buffers: step i + 1's inputs
+    # go in (one stream, in the order the calls need them) while step i computes
+    # (the compute stream) and its results come out (a third stream, each tensor
+    # as soon as the call that writes it is done).  A set is reused only after
+    # the step two back has finished reading its inputs and its results are out.
+    # No L2 flush: each step's 138 MB of inputs exceeds L2.  The timed region runs
+    # from before the first copy in to after the last copy out.
     s_in = torch.cuda.Stream(device)
     s_out = torch.cuda.Stream(device)
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+
+    def dev_set():
+        d = {k: torch.empty_like(v) for k, v in dev_in.items()}
+        d.update({k: torch.empty_like(v) for k, v in dev_out.items()})
+        d["u"] = torch.empty_like(u)
+        d["mean"] = torch.empty_like(mean)
+        d["rstd"] = torch.empty_like(rstd)
+        d["ws_bwd"] = torch.empty_like(ws_bwd)
+        d["ws_proj"] = torch.empty_like(ws_proj)
+        return d
+
+    sets = [dev_set(), dev_set()]
 
     def ev(st):
         e = torch.cuda.Event()
         e.record(st)
         return e
 
+    free_in = [None, None]   # event: the set's inputs are no longer read
+    free_out = [None, None]  # event: the set's results have been copied out
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    stream.wait_event(t0)
+    s_out.wait_event(t0)
     for i in range(K3):
-        flush()
-        s_in.wait_event(ev(stream))
-        e0[i].record(s_in)
+        d = sets[i % 2]
+        if free_in[i % 2] is not None:
+            s_in.wait_event(free_in[i % 2])
         with torch.cuda.stream(s_in):
             for k in ("temb", "W", "b"):
-                dev_in[k].copy_(pin[k], non_blocking=True)
+                d[k].copy_(pin[k], non_blocking=True)
             e_proj = ev(s_in)
-            dev_in["x"].copy_(pin["x"], non_blocking=True)
+            d["x"].copy_(pin["x"], non_blocking=True)
             e_x = ev(s_in)
-            dev_in["dy"].copy_(pin["dy"], non_blocking=True)
+            d["dy"].copy_(pin["dy"], non_blocking=True)
             e_dy = ev(s_in)
+        if free_out[i % 2] is not None:
+            stream.wait_event(free_out[i % 2])
         stream.wait_event(e_proj)
-        binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=stream)
+        binding.adaln_proj_fwd(d["temb"], d["W"], d["b"], emb=d["emb"], u=d["u"], stream=stream)
         stream.wait_event(e_x)
-        binding.adaln_out_fwd(x, emb, out=out, mean=mean, rstd=rstd, stream=stream)
+        binding.adaln_out_fwd(d["x"], d["emb"], out=d["out"], mean=d["mean"], rstd=d["rstd"], stream=stream)
         e_fwd = ev(stream)
         stream.wait_event(e_dy)
-        binding.adaln_out_bwd(dy, x, emb, mean, rstd, dx=dx, d_emb=d_emb, workspace=ws_bwd, stream=stream)
+        binding.adaln_out_bwd(d["dy"], d["x"], d["emb"], d["mean"], d["rstd"], dx=d["dx"], d_emb=d["d_emb"],
+                              workspace=d["ws_bwd"], stream=stream)
         e_bwd = ev(stream)
-        binding.adaln_proj_bwd(d_emb, temb, u, W, d_temb=d_temb, dW=dW, db=db, workspace=ws_proj, stream=stream)
+        binding.adaln_proj_bwd(d["d_emb"], d["temb"], d["u"], d["W"], d_temb=d["d_temb"], dW=d["dW"], db=d["db"],
+                               workspace=d["ws_proj"], stream=stream)
         e_end = ev(stream)
+        free_in[i % 2] = e_end
         with torch.cuda.stream(s_out):
             s_out.wait_event(e_fwd)
             for k in ("out", "emb"):
-                outs_h[k].copy_(dev_out[k], non_blocking=True)
+                outs_h[k].copy_(d[k], non_blocking=True)
             s_out.wait_event(e_bwd)
             for k in ("dx", "d_emb"):
-                outs_h[k].copy_(dev_out[k], non_blocking=True)
+                outs_h[k].copy_(d[k], non_blocking=True)
             s_out.wait_event(e_end)
             for k in ("d_temb", "dW", "db"):
-                outs_h[k].copy_(dev_out[k], non_blocking=True)
-            e1[i].record(s_out)
-        stream.wait_event(e1[i])
+                outs_h[k].copy_(d[k], non_blocking=True)
+            free_out[i % 2] = ev(s_out)
+    t1.record(s_out)
     torch.cuda.synchronize()
-    e2e_s = sum(a.elapsed_time(c) for a, c in zip(e0, e1)) / 1e3
+    e2e_s = t0.elapsed_time(t1) / 1e3
+    # the last step's results equal the ones computed in place
+    assert torch.equal(outs_h["dW"].view(torch.int16), dW.cpu().view(torch.int16))
     e2e_max = max_over_ranks(e2e_s, dist_mod, device)
     assert binding.device_error() == 0
 
