@@ -40,7 +40,7 @@ KERNELS_PER_STEP = 7  # SiLU, projection, out_fwd, bwd tile, tree fold, proj-bwd
 # DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold) at this
 # workload, from the ncu capture summarised in profiles/out_bwd_B2_S4096_D3072.md.  The
 # counters of a replayed launch miss the dx lines still in L2 when it ends.
-OUT_BWD_DRAM_BYTES = 133_250_000
+OUT_BWD_DRAM_BYTES = 133_192_704
 
 
 # ---------------------------------------------------------------------------
