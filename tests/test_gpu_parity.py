@@ -71,6 +71,27 @@ def test_silu_every_bf16_input():
     assert_bitwise(host_bf16(u), oracle.silu_bf16(temb), "silu over all bf16")
 
 
+@pytest.mark.parametrize("B,D", [(2, 4096), (2, 3072), (1, 3072)])
+def test_silu_every_bf16_input_small_batch(B, D):
+    """The same 65536 patterns through the one- and two-sample projection
+    (the streaming kernel, and D = 4096 beyond its register budget): u bit
+    for bit, and emb = bf16(bias) exactly when W is zero."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    allb[(allb & 0x7F80) == 0x7F80] = 0
+    n = B * D
+    chunks = (allb.size + n - 1) // n
+    padded = np.zeros(chunks * n, np.uint16)
+    padded[:allb.size] = allb
+    W = dev_bf16(np.zeros((2 * D, D), np.uint16))
+    bias = np.arange(2 * D, dtype=np.uint16) % 0x3F00
+    bd = dev_bf16(bias)
+    for c in range(chunks):
+        temb = padded[c * n:(c + 1) * n].reshape(B, D)
+        emb, u = binding.adaln_proj_fwd(dev_bf16(temb), W, bd)
+        assert_bitwise(host_bf16(u), oracle.silu_bf16(temb), f"silu chunk {c}")
+        assert_bitwise(host_bf16(emb), np.broadcast_to(bias, (B, 2 * D)), f"emb chunk {c}")
+
+
 def test_proj_fwd_weight_zero_gives_bias():
     inp = synth.make_inputs(3, 1, 3072, 7)
     emb, _ = binding.adaln_proj_fwd(dev_bf16(inp["temb"]), dev_bf16(np.zeros_like(inp["W"])), dev_bf16(inp["b"]))
