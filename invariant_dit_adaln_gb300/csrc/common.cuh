@@ -132,15 +132,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// two sums at once (each with the butterfly of warp_sum)
-__device__ __forceinline__ float2 warp_sum2(float2 v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float2 o = make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.x, off), __shfl_xor_sync(0xFFFFFFFFu, v.y, off));
-        v = f2add(v, o);
-    }
-    return v;
-}
 
 // --------------------------------------------------------------------------
 // shared memory, mbarriers, bulk copies (the TMA engine), PDL
