@@ -527,7 +527,8 @@ def run_reference(args, world, rank):
     total = sum(times)
     tokens = B * S * frac * len(times)
     value = tokens / total
-    sample = (f"each step: the oracle chain on {frac:g} of the workload (first {max(1, int(round(S * frac)))} "
+    part = "the whole workload" if frac >= 1.0 else f"a fraction {frac:g} of the workload"
+    sample = (f"each step: the oracle chain on {part} (first {max(1, int(round(S * frac)))} "
               f"tokens of each of B={B} samples, {max(1, int(round(2 * D * frac)))} of {2 * D} projection rows), "
               f"single thread")
     return {
