@@ -146,10 +146,15 @@ size_t adaln_out_bwd_workspace_bytes(int B, int S, int D);
  * (PR 538 "What": LayerNorm backward per row; d_scale, d_shift as token sums
  * in the fixed 32-way tree).
  *
- *   g     = fp32(dy);  gh = g * onep (exact);  xhat as in the forward, from the
- *           saved mean/rstd, bit-identical to the forward's value
+ *   g     = fp32(dy);  gh = g * onep (exact unless it underflows);  xhat as in
+ *           the forward, from the saved mean/rstd, bit-identical to the
+ *           forward's value
  *   dx    = bf16( rstd * ((gh - c1) - xhat * c2) ),  c1 = sum_d gh / D,
- *           c2 = sum_d gh*xhat / D   (fixed-order fp32 reductions over d)
+ *           c2 = sum_d gh*xhat / D   (fixed-order fp32 reductions over d, each
+ *           sum times the correctly rounded 1/D).  The same quantity is
+ *           evaluated as rstd*gh - rstd*c1 + (mean - x)*rstd^2*c2 with two
+ *           fused multiply-adds, so dx is within the rounding error of this
+ *           formula, not bit-identical to one fixed evaluation of it.
  *   d_emb[b, 0:D]  = d_scale = tree_s( fp32(g * xhat) )
  *   d_emb[b, D:2D] = d_shift = tree_s( g )
  *
