@@ -9,6 +9,7 @@ of the dominant call, an end-to-end number through host buffers, the CPU
 oracle's throughput and the SM clocks seen during the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --proj-sweep      # the projection calls alone, B = 1 .. 2048
 
 Under torchrun (N > 1) every rank runs its own replica (weak scaling; the
 path has no cross-sample exchange), the elapsed time is the max over ranks
@@ -552,6 +553,67 @@ def run_reference(args, world, rank):
     }
 
 
+def run_proj_sweep(args, rank, local):
+    """The two projection calls alone over the conditioning batch B (D = 3072,
+    weights N(0, 0.02^2)): each call timed by CUDA events on its stream, the
+    median of several runs, L2 flushed before each.  One JSON line per B, on
+    rank 0; a diagnostic of how the CUDA-core projections grow with B, not
+    the headline."""
+    if rank != 0:
+        return
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    build.build()
+    binding.load()
+    D = WORKLOAD["D"]
+    N = 2 * D
+    host = synth.make_inputs(2048, 1, D, seed=WORKLOAD["seed"])
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    W, b, temb_all = dev(host["W"]), dev(host["b"]), dev(host["temb"])
+    d_emb_all = torch.from_numpy(synth.normal(synth.stream_key(WORKLOAD["seed"], "aux"), 2048 * N)
+                                 .astype(np.float32).reshape(2048, N)).to(device)
+    dW = torch.empty((N, D), dtype=torch.bfloat16, device=device)
+    db = torch.empty((N,), dtype=torch.bfloat16, device=device)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    st = torch.cuda.current_stream(device)
+    for B in [1, 2, 8, 64, 257, 2048]:
+        temb, d_emb = temb_all[:B].contiguous(), d_emb_all[:B].contiguous()
+        emb = torch.empty((B, N), dtype=torch.bfloat16, device=device)
+        u = torch.empty((B, D), dtype=torch.bfloat16, device=device)
+        d_temb = torch.empty((B, D), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(max(1, binding.adaln_proj_bwd_workspace_bytes(B, D)), dtype=torch.uint8, device=device)
+        calls = {"adaln_proj_fwd": lambda: binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=st),
+                 "adaln_proj_bwd": lambda: binding.adaln_proj_bwd(d_emb, temb, u, W, d_temb=d_temb, dW=dW, db=db,
+                                                                  workspace=ws, stream=st)}
+        runs = 20 if B >= 257 else 100
+        res = {}
+        for name, call in calls.items():
+            call()
+            torch.cuda.synchronize(device)
+            ts = []
+            for _ in range(runs):
+                flush_w.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                call()
+                e1.record(st)
+                torch.cuda.synchronize(device)
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            res[name] = statistics.median(ts)
+        if binding.device_error() != 0:
+            raise RuntimeError("device-side error during the projection sweep")
+        flops = {"adaln_proj_fwd": 2.0 * B * N * D, "adaln_proj_bwd": 4.0 * B * N * D}
+        print(json.dumps({"sweep": "projections", "B": B, "D": D, "us": res,
+                          "tflops": {k: flops[k] / (v * 1e-6) / 1e12 for k, v in res.items()},
+                          "runs": runs, "l2": "512 MiB write before each run"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -562,10 +624,15 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm's steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time the step as separate calls, not a CUDA graph")
+    ap.add_argument("--proj-sweep", action="store_true",
+                    help="instead of the step: time the projection calls alone for B = 1 .. 2048")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
+    if args.proj_sweep:
+        run_proj_sweep(args, rank, local)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
     else:
