@@ -66,6 +66,86 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return _
 __device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
 
 // --------------------------------------------------------------------------
+// Packed fp32x2 in inline PTX, on a 64-bit register pair {lo, hi}.
+//
+// Every operation names its rounding (.rn), and PTX never contracts a
+// multiply or an add that carries an explicit rounding into a fused
+// multiply-add, so a product written here is always rounded before the add
+// that consumes it.  On this GPU a packed instruction occupies the FMA pipe for
+// two cycles (it does two lanes of work), so packing halves the issue slots of
+// fp32 arithmetic without changing its pipe time.
+// --------------------------------------------------------------------------
+typedef unsigned long long px2;
+
+__device__ __forceinline__ px2 px_add(px2 a, px2 b) {
+    px2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ px2 px_sub(px2 a, px2 b) {
+    px2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ px2 px_mul(px2 a, px2 b) {
+    px2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ px2 px_fma(px2 a, px2 b, px2 c) {
+    px2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ px2 px_make(float lo, float hi) {
+    px2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ px2 px_splat(float a) { return px_make(a, a); }
+__device__ __forceinline__ float px_lo(px2 a) {
+    float l;
+    asm("{.reg .b32 h;\n\tmov.b64 {%0, h}, %1;}" : "=f"(l) : "l"(a));
+    return l;
+}
+__device__ __forceinline__ float px_hi(px2 a) {
+    float h;
+    asm("{.reg .b32 l;\n\tmov.b64 {l, %0}, %1;}" : "=f"(h) : "l"(a));
+    return h;
+}
+// a packed bf16x2 word (lo in the low half) as the exact fp32 pair, on the
+// integer pipe: the low half moved up by a byte permute, the high half masked
+__device__ __forceinline__ px2 px_bf16(uint32_t w) {
+    px2 d;
+    asm("{.reg .b32 l, h;\n\t"
+        "prmt.b32 l, %1, 0, 0x1044;\n\t"
+        "and.b32 h, %1, 0xFFFF0000;\n\t"
+        "mov.b64 %0, {l, h};}"
+        : "=l"(d)
+        : "r"(w));
+    return d;
+}
+// a pair rounded to a packed bf16x2 word (round to nearest even), lo low
+__device__ __forceinline__ uint32_t px_to_bf16x2(px2 a) {
+    uint32_t o;
+    asm("{.reg .b32 l, h;\n\t"
+        "mov.b64 {l, h}, %1;\n\t"
+        "cvt.rn.bf16x2.f32 %0, h, l;}"
+        : "=r"(o)
+        : "l"(a));
+    return o;
+}
+// Knuth's TwoSum on both lanes: t = s + v and the exact error e of that add
+// (s + v = t + e); then c += e and s = t.  Seven packed operations.
+__device__ __forceinline__ void px_twosum(px2 &s, px2 &c, px2 v) {
+    const px2 t = px_add(s, v);
+    const px2 bp = px_sub(t, s);
+    const px2 e = px_add(px_sub(s, px_sub(t, bp)), px_sub(v, bp));
+    c = px_add(c, e);
+    s = t;
+}
+
+// --------------------------------------------------------------------------
 // SiLU rounded to bf16: the nearest bf16 to the fp64 value of t/(1+exp(-t)).
 // Computed in fp32 (error below 4 fp32 ulps); when the fp32 value lies within
 // 16 fp32 ulps of a bf16 rounding midpoint, or exp(-t) would overflow fp32,
@@ -178,6 +258,54 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// A wait that sleeps between tries (waiting warps take no issue slots) and
+// also gives up as soon as *abort is non-zero (another warp of the CTA gave up
+// first) or after `limit_ns`.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                   uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// plain arrival on an mbarrier (release semantics at CTA scope)
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// atomic add on shared memory with acquire-release semantics at CTA scope:
+// the caller's earlier accesses are ordered before it, and the accesses of
+// the threads whose additions it observes are visible after it.  Returns the
+// old value.
+__device__ __forceinline__ unsigned smem_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
+// order this thread's (and, after an acquire, the CTA's) generic-proxy
+// accesses of shared memory before later async-proxy (bulk copy) accesses
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared through the TMA engine, completing on `bar`.

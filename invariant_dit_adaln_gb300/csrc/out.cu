@@ -483,38 +483,79 @@ cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out
 // ==========================================================================
 // Backward, kernel 1: one CTA per (sample b, 32-token tile t).
 //
-// Thread i owns the 16-byte vectors v = i + NT j (8 columns each).  Rows
-// arrive through a ring of bulk copies (an x row and a dy row per stage) and
-// are taken in blocks of kRowBlock rows.  Phase 1, per row in ascending s:
-// x_hat = (x - mean) * rstd (bit-identical to the forward's), g = fp32(dy),
-// gh = g * onep; the row's products g * x_hat and g go into the columns' tree
-// accumulators (the tile's level-0 node), and each thread keeps its partial
-// sums of gh and gh * x_hat (column pairs in packed fp32x2, the two halves);
-// after the block's rows each warp reduces all of them at once (a fixed
-// transposed butterfly) and publishes them.  After one barrier, one thread per row adds the warps'
-// partials in ascending warp order, giving c1 and c2.  Phase 2 recomputes gh
-// and x - mean from the staged rows and writes dx = rstd * (gh - c1 - x_hat *
-// c2), evaluated as rstd gh - rstd c1 + (mean - x) rstd^2 c2 with two fused
-// multiply-adds per column pair.  The reduction order over d depends on D only.
+// Thread i owns the 16-byte vectors v = i + NT j (8 columns each); all its
+// fp32 arithmetic is packed (column pairs), in inline PTX with explicit
+// rounding, so no product is ever fused into the add that consumes it.  Rows
+// arrive through a ring of NST stages (an x row and a dy row each) filled by
+// bulk copies, and are taken in blocks of RB rows.
+//
+// Phase 1, per row in ascending s: x_hat = (x - mean) * rstd (bit-identical to
+// the forward's value), g = fp32(dy), the token product p = g * x_hat (rounded);
+// p and g go into the columns' level-0 tree nodes by TwoSum (the Neumaier step,
+// branch-free), and each thread keeps partial row sums of g * onep and
+// p * onep.  The warp reduces the block's sums at once (column pairs' halves,
+// then a fixed transposed butterfly) and publishes them; after one CTA barrier
+// every warp adds the warps' sums in ascending order (every warp the same
+// bits): c1 = sum_d g onep / D, c2 = sum_d g x_hat onep / D.  Phase 2 writes
+//     dx = rstd gh + (mean rstd^2 c2 - rstd c1) - x rstd^2 c2,   gh = g * onep,
+// which is rstd (gh - c1 - x_hat c2), two fused multiply-adds per column pair
+// after one multiply.  The reduction order over d depends on D only.  A block's
+// stages are refilled by the last warp to finish its phase 2 (a counter per
+// block of stages), while the other warps go on.
 // ==========================================================================
-constexpr int kRowBlock = 4;    // most rows per block (a block of RB rows, NST = 2 RB stages:
-                                // two blocks of rows in flight)
+constexpr int kRowBlock = 4;        // most rows per block
+constexpr int kBwdMaxStages = 8;
 
 struct BwdSmem {
-    float2 red[kRowBlock][32];  // [row of the block][warp] = (sum gh, sum gh * x_hat)
-    float2 tot[kRowBlock];      // [row of the block] = (c1, c2)
+    float2 red[2][kRowBlock][32];   // [block parity][row of the block][warp] = (sum g onep, sum p onep)
     float mu[kTile], rs[kTile];
-    uint64_t full[2 * kRowBlock];
+    uint64_t full[kBwdMaxStages];   // a stage's copies have landed
+    unsigned rel[kBwdMaxStages];    // warps done with the rows of a block of stages
+    int last[kBwdMaxStages];        // latest row copied into a stage (-1: none)
+    int abort;                      // a wait ran out of time
 };
 
-template <int VPT, int MAXNT, int MINB, int RB, int NST>
+// The NV partial sums of a warp's lanes reduced at once (a transposed
+// butterfly): at the first log2(NV) levels a lane keeps half of its values and
+// adds the partner's copy of them, then plain levels follow; lane l ends with
+// value l >> (5 - log2 NV) summed over all 32 lanes, in a fixed tree.
+template <int NV>
+__device__ __forceinline__ float warp_transposed_sum(const float (&in)[NV], int lane) {
+    static_assert(NV == 2 || NV == 4 || NV == 8, "2, 4 or 8 values");
+    float a[NV];
+#pragma unroll
+    for (int q = 0; q < NV; ++q) a[q] = in[q];
+#pragma unroll
+    for (int off = 16, cnt = NV; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int q = 0; q < NV / 2; ++q) {
+                if (q < cnt / 2) {
+                    const float keep = up ? a[q + cnt / 2] : a[q];
+                    const float give = up ? a[q] : a[q + cnt / 2];
+                    a[q] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, off));
+                }
+            }
+            cnt /= 2;
+        } else {
+            a[0] = __fadd_rn(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], off));
+        }
+    }
+    return a[0];
+}
+
+template <int VPT, int MAXNT, int MINB, int RB, int NST, bool EXACT>
 __global__ void __launch_bounds__(MAXNT, MINB)
 out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
                     const uint16_t *__restrict__ emb, const float *__restrict__ mean,
                     const float *__restrict__ rstd, uint16_t *__restrict__ dx, float *__restrict__ ws_sig,
                     float *__restrict__ ws_kap, int S, int D, int T) {
+    static_assert((RB == 1 || RB == 2 || RB == 4) && NST >= 2 * RB && NST <= kBwdMaxStages && NST % RB == 0,
+                  "whole blocks of rows per stage group, two blocks in flight");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     BwdSmem &sm = *reinterpret_cast<BwdSmem *>(smem_raw);
+    volatile int *abort_flag = &sm.abort;
     unsigned char *stages = smem_raw + ((sizeof(BwdSmem) + 127) / 128) * 128;
     const int row_bytes = D * 2;
     const int stage_bytes = 2 * row_bytes;  // x row, then dy row
@@ -532,7 +573,12 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
     const size_t row0 = (size_t)b * S + s0;
 
     if (tid == 0) {
-        for (int s = 0; s < NST; ++s) mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&sm.full[s], 1);
+            sm.rel[s] = 0u;
+            sm.last[s] = -1;
+        }
+        sm.abort = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -551,7 +597,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
-        sc_v[j] = v < V ? ldg16(e + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
+        sc_v[j] = (EXACT || v < V) ? ldg16(e + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
         for (int i = 0; i < NST && i < n; ++i) {
@@ -559,185 +605,195 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             mbar_arrive_expect_tx(&sm.full[i], stage_bytes);
             bulk_g2s(dst, x + (row0 + i) * D, row_bytes, &sm.full[i]);
             bulk_g2s(dst + row_bytes, dy + (row0 + i) * D, row_bytes, &sm.full[i]);
+            sm.last[i] = i;
         }
     }
     if (tid < n) {
         sm.mu[tid] = mu_t;
         sm.rs[tid] = rs_t;
     }
-    float2 onep[VPT][4];
+    // onep = bf16(fp32(1 + scale)) of this thread's columns, by column pair
+    px2 onep[VPT][4];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int v = tid + NT * j;
-        if (v < V) {
-            const uint4 sc = sc_v[j];
-            const uint32_t w[4] = {sc.x, sc.y, sc.z, sc.w};
+        const uint32_t w[4] = {sc_v[j].x, sc_v[j].y, sc_v[j].z, sc_v[j].w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f = bf16x2_to_f2(w[q]);
-                onep[j][q] = make_float2(bf16f(bf16_bits(__fadd_rn(1.0f, f.x))), bf16f(bf16_bits(__fadd_rn(1.0f, f.y))));
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) onep[j][q] = make_float2(0.0f, 0.0f);
-        }
+        for (int q = 0; q < 4; ++q)
+            onep[j][q] = px_make(bf16f(bf16_bits(__fadd_rn(1.0f, bf16lo(w[q])))),
+                                 bf16f(bf16_bits(__fadd_rn(1.0f, bf16hi(w[q])))));
     }
     __syncthreads();
 
-    // Tree nodes of the scale products g * x_hat and of the shift products g, by
-    // column pair.  They start at +0 rather than at the first token: adding a
-    // value v to +0 gives v exactly with no error, so every later step is the
-    // same; only an all-zero column can differ, in the sign of its level-0 sum
-    // (+0 for -0), and its root (sum + correction) is +0 either way.
-    float2 sg_s[VPT][4], kp_s[VPT][4], sg_h[VPT][4], kp_h[VPT][4];
+    // Tree nodes of the scale products p = g * x_hat and of the shift products
+    // g, by column pair.  They start at +0 rather than at the first token:
+    // adding a value v to +0 gives v exactly with no error, so every later step
+    // is the same; only an all-zero column can differ, in the sign of its
+    // level-0 sum (+0 for -0), and its root (sum + correction) is +0 either way.
+    px2 sg_s[VPT][4], kp_s[VPT][4], sg_h[VPT][4], kp_h[VPT][4];
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            sg_s[j][q] = kp_s[j][q] = sg_h[j][q] = kp_h[j][q] = make_float2(0.0f, 0.0f);
-        }
+        for (int q = 0; q < 4; ++q) sg_s[j][q] = kp_s[j][q] = sg_h[j][q] = kp_h[j][q] = 0ull;
     const float invD = __frcp_rn((float)D);  // c1, c2 only feed dx (tolerance-checked)
 
-    for (int r0 = 0; r0 < n; r0 += RB) {
-        const int nb = min(RB, n - r0);
-        // ---- phase 1: tree products and the row sums ----
-        bool ok = true;
-        float rsum[2 * kRowBlock];  // this thread's (sum gh, sum gh * x_hat) of each row of the block
+    // phase 1 of one row, its sums into rsum[2 jr], rsum[2 jr + 1]; EXACT: every
+    // thread's vectors lie inside the row (no bounds test, so the tree state
+    // stays in the same registers on every path)
+    auto phase1_row = [&](int i, int jr, float (&rsum)[2 * RB]) {
+        const unsigned char *xs = stages + (size_t)(i % NST) * stage_bytes;
+        const unsigned char *gs = xs + row_bytes;
+        const px2 mu2 = px_splat(sm.mu[i]), rs2 = px_splat(sm.rs[i]);
+        px2 a1 = 0ull, a2 = 0ull;
 #pragma unroll
-        for (int q = 0; q < 2 * kRowBlock; ++q) rsum[q] = 0.0f;
-        #pragma unroll
-        for (int jr = 0; jr < RB; ++jr) if (jr < nb) {
-            const int i = r0 + jr;
-            const int st = i % NST;
-            ok = mbar_wait_bounded(&sm.full[st], (uint32_t)(i / NST) & 1u) && ok;
-            const unsigned char *xs = stages + (size_t)st * stage_bytes;
-            const unsigned char *gs = xs + row_bytes;
-            const float2 mu2 = f2splat(sm.mu[i]), rs2 = f2splat(sm.rs[i]);
-            float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tid + NT * j;
-                if (v < V && ok) {
-                    const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
-                    const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
-                    const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
-                    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 g2 = bf16x2_to_f2(ga[q]);
-                        const float2 xh = f2mul(f2sub(bf16x2_to_f2(xa[q]), mu2), rs2);
-                        const float2 gh = f2mul(g2, onep[j][q]);
-                        a1 = f2add(a1, gh);
-                        a2 = f2fma(gh, xh, a2);
-                        // the token product g * x_hat is rounded before it enters the tree
-                        const float2 ps = make_float2(__fmul_rn(g2.x, xh.x), __fmul_rn(g2.y, xh.y));
-                        // scalar TwoSum for the scale tree (its products are scalar already):
-                        // the scalar ops can use both FMA pipes, the packed ones only one
-                        twosum(sg_s[j][q].x, kp_s[j][q].x, ps.x);
-                        twosum(sg_s[j][q].y, kp_s[j][q].y, ps.y);
-                        twosum2(sg_h[j][q], kp_h[j][q], g2);
-                    }
-                }
-            }
-            rsum[2 * jr] = __fadd_rn(a1.x, a1.y);
-            rsum[2 * jr + 1] = __fadd_rn(a2.x, a2.y);
-        }
-        {
-            // The block's 2 RB sums over the warp's 32 lanes at once (a transposed
-            // butterfly): at each of the first levels a lane keeps half of its
-            // values and adds the partner's copy of them; after the last level
-            // lane l holds value (l >> 2) summed over all lanes, in a fixed tree.
-            static_assert(RB == 4 || RB == 2, "blocks of 2 or 4 rows");
-            float w4[4], w2[2];
-            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-            if (RB == 4) {
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + NT * j;
+            if (EXACT || v < V) {
+                const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
+                const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
+                const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
+                const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float keep = b4 ? rsum[q + 4] : rsum[q], give = b4 ? rsum[q] : rsum[q + 4];
-                    w4[q] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 16));
+                    const px2 g2 = px_bf16(ga[q]);
+                    const px2 xh = px_mul(px_sub(px_bf16(xa[q]), mu2), rs2);  // x_hat
+                    const px2 p = px_mul(g2, xh);  // rounded before it enters the tree
+                    a1 = px_fma(g2, onep[j][q], a1);
+                    a2 = px_fma(p, onep[j][q], a2);
+                    px_twosum(sg_s[j][q], kp_s[j][q], p);
+                    px_twosum(sg_h[j][q], kp_h[j][q], g2);
                 }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) w4[q] = __fadd_rn(rsum[q], __shfl_xor_sync(0xFFFFFFFFu, rsum[q], 16));
             }
+        }
+        rsum[2 * jr] = __fadd_rn(px_lo(a1), px_hi(a1));
+        rsum[2 * jr + 1] = __fadd_rn(px_lo(a2), px_hi(a2));
+    };
+    // phase 2 of one row: dx from the row's constants k2 = rstd^2 c2 and
+    // k3 = mean k2 - rstd c1
+    auto phase2_row = [&](int i, float k2, float k3) {
+        const unsigned char *xs = stages + (size_t)(i % NST) * stage_bytes;
+        const unsigned char *gs = xs + row_bytes;
+        const px2 rs2 = px_splat(sm.rs[i]), nk2 = px_splat(-k2), k3v = px_splat(k3);
+        uint16_t *drow = dx + (row0 + i) * D;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float keep = b3 ? w4[q + 2] : w4[q], give = b3 ? w4[q] : w4[q + 2];
-                w2[q] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 8));
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + NT * j;
+            if (EXACT || v < V) {
+                const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
+                const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
+                const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
+                const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const px2 gh = px_mul(px_bf16(ga[q]), onep[j][q]);
+                    const px2 t = px_fma(px_bf16(xa[q]), nk2, k3v);
+                    o[q] = px_to_bf16x2(px_fma(gh, rs2, t));
+                }
+                stg16(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
             }
-            const float keep = b2 ? w2[1] : w2[0], give = b2 ? w2[0] : w2[1];
-            float v = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 4));
-            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
-            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
-            // value index: (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0) = 2 jr + quantity (RB == 4);
-            // with RB == 2 the upper half is never kept and lanes 0-15 hold the values
-            const int idx = (lane >> 2) & 7;
-            if ((lane & 3) == 0 && idx < 2 * RB) {
-                float *dst = reinterpret_cast<float *>(&sm.red[idx >> 1][warp]);
+        }
+    };
+
+    const int nblk = (n + RB - 1) / RB;
+    bool ok = true;
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int r0 = blk * RB;
+        const int nb = min(RB, n - r0);
+        // ---- phase 1: tree products and the row sums ----
+        bool landed = true;
+#pragma unroll
+        for (int jr = 0; jr < RB; ++jr)
+            if (jr < nb)
+                landed = mbar_wait_or_abort(&sm.full[(r0 + jr) % NST], (uint32_t)((r0 + jr) / NST) & 1u,
+                                            abort_flag) && landed;
+        landed = __all_sync(0xFFFFFFFFu, landed);
+        float rsum[2 * RB];  // this thread's (sum g onep, sum p onep) of each row of the block
+#pragma unroll
+        for (int q = 0; q < 2 * RB; ++q) rsum[q] = 0.0f;
+        if (landed) {
+            if (nb == RB) {
+#pragma unroll
+                for (int jr = 0; jr < RB; ++jr) phase1_row(r0 + jr, jr, rsum);
+            } else {  // the short last block of a ragged tile
+#pragma unroll
+                for (int jr = 0; jr < RB; ++jr)
+                    if (jr < nb) phase1_row(r0 + jr, jr, rsum);
+            }
+        }
+        // publish the warp's sums of the block: lane l holds value l >> (5 - log2(2 RB))
+        {
+            const float v = warp_transposed_sum<2 * RB>(rsum, lane);
+            constexpr int kShift = RB == 4 ? 2 : (RB == 2 ? 3 : 4);
+            const int idx = lane >> kShift;
+            if ((lane & ((1 << kShift) - 1)) == 0) {
+                float *dst = reinterpret_cast<float *>(&sm.red[blk & 1][idx >> 1][warp]);
                 dst[idx & 1] = v;
             }
         }
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                report_error(kErrOutBwdWait);
-                // let the copies this CTA issued finish before leaving
-                const int issued = min(n, r0 + NST);
-                for (int k = r0; k < issued; ++k)
-                    mbar_wait_bounded(&sm.full[k % NST], (uint32_t)(k / NST) & 1u, 10000000ull);
-            }
-            return;
+        if (__syncthreads_or(!landed)) {
+            ok = false;
+            break;
         }
-        if (tid < nb) {
-            float2 c = sm.red[tid][0];
-            for (int w = 1; w < nwarps; ++w) c = f2add(c, sm.red[tid][w]);
-            // dx = rstd (gh - c1 - x_hat c2) = rstd gh - rstd c1 + (mean - x) rstd^2 c2
-            const float rsv = sm.rs[r0 + tid];
-            const float c1 = __fmul_rn(c.x, invD), c2 = __fmul_rn(c.y, invD);
-            sm.tot[tid] = make_float2(__fmul_rn(rsv, c1), __fmul_rn(__fmul_rn(rsv, rsv), c2));
-        }
-        __syncthreads();
         // ---- phase 2: dx ----
-        #pragma unroll
-        for (int jr = 0; jr < RB; ++jr) if (jr < nb) {
-            const int i = r0 + jr;
-            const unsigned char *xs = stages + (size_t)(i % NST) * stage_bytes;
-            const unsigned char *gs = xs + row_bytes;
-            const float2 mu2 = f2splat(sm.mu[i]), rs2 = f2splat(sm.rs[i]);
-            const float2 c = sm.tot[jr];
-            const float2 na = f2splat(-c.x), c2r = f2splat(c.y);
-            uint16_t *drow = dx + (row0 + i) * D;
+        // lane l < 2 nb: quantity (l & 1) of row (l >> 1), the warps added in ascending order
+        float cs = 0.0f;
+        if (lane < 2 * nb) {
+            const float *src = reinterpret_cast<const float *>(&sm.red[blk & 1][lane >> 1][0]) + (lane & 1);
+            cs = src[0];
+            for (int w = 1; w < nwarps; ++w) cs = __fadd_rn(cs, src[2 * w]);
+            cs = __fmul_rn(cs, invD);
+        }
+        // dx = rstd (gh - c1 - x_hat c2) = rstd gh + (mean k2 - rstd c1) - x k2,  k2 = rstd^2 c2
+        const float c2 = __shfl_down_sync(0xFFFFFFFFu, cs, 1);
+        float k2 = 0.0f, k3 = 0.0f;
+        if ((lane & 1) == 0 && lane < 2 * nb) {
+            const float rsv = sm.rs[r0 + (lane >> 1)], muv = sm.mu[r0 + (lane >> 1)];
+            k2 = __fmul_rn(__fmul_rn(rsv, rsv), c2);
+            k3 = __fmaf_rn(muv, k2, -__fmul_rn(rsv, cs));
+        }
+        if (nb == RB) {
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tid + NT * j;
-                if (v < V) {
-                    const uint4 xw = *reinterpret_cast<const uint4 *>(xs + (size_t)v * 16);
-                    const uint4 gw = *reinterpret_cast<const uint4 *>(gs + (size_t)v * 16);
-                    const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w};
-                    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
-                    uint32_t o[4];
+            for (int jr = 0; jr < RB; ++jr)
+                phase2_row(r0 + jr, __shfl_sync(0xFFFFFFFFu, k2, 2 * jr), __shfl_sync(0xFFFFFFFFu, k3, 2 * jr));
+        } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 xm = f2sub(mu2, bf16x2_to_f2(xa[q]));
-                        const float2 gh = f2mul(bf16x2_to_f2(ga[q]), onep[j][q]);
-                        const float2 d = f2fma(xm, c2r, f2fma(rs2, gh, na));
-                        o[q] = pack_bf16x2(d.x, d.y);
+            for (int jr = 0; jr < RB; ++jr) {
+                const float kk2 = __shfl_sync(0xFFFFFFFFu, k2, 2 * jr), kk3 = __shfl_sync(0xFFFFFFFFu, k3, 2 * jr);
+                if (jr < nb) phase2_row(r0 + jr, kk2, kk3);
+            }
+        }
+        // this warp is done with the block's stages; the last warp to finish
+        // refills them with the rows NST further on
+        __syncwarp();
+        if (lane == 0) {
+            const int grp = blk % (NST / RB);
+            if (smem_add_acq_rel(&sm.rel[grp], 1u) == (unsigned)nwarps - 1u) {
+                sm.rel[grp] = 0u;
+                fence_proxy_async_smem();
+                for (int jr = 0; jr < nb; ++jr) {
+                    const int i = r0 + jr;
+                    const int st = i % NST;
+                    if (i + NST < n) {
+                        unsigned char *dst = stages + (size_t)st * stage_bytes;
+                        mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
+                        bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                        bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                        sm.last[st] = i + NST;
                     }
-                    stg16(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
                 }
             }
         }
-        __syncthreads();  // every thread is done with this block's stages
-        // lanes 0 .. nb-1 of warp 0 re-arm one stage each (each stage has its own barrier)
-        if (tid < nb) {
-            const int i = r0 + tid;
-            if (i + NST < n) {
-                const int st = i % NST;
-                unsigned char *dst = stages + (size_t)st * stage_bytes;
-                mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
-                bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
-                bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
-            }
+    }
+    if (!ok) {
+        // every thread left the loop at the same barrier: no copy is issued any more
+        if (tid == 0) {
+            report_error(kErrOutBwdWait);
+            // let the copies this CTA issued land before it leaves
+            for (int st = 0; st < NST; ++st)
+                if (sm.last[st] >= 0)
+                    mbar_wait_bounded(&sm.full[st], (uint32_t)(sm.last[st] / NST) & 1u, 10000000ull);
         }
+        return;
     }
     // level-0 node of this tile: scale half at columns [0, D), shift half at [D, 2D)
     const int H = 2 * D;
@@ -746,16 +802,18 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
-        if (v < V) {
+        if (EXACT || v < V) {
             const size_t c = (size_t)v * 8;
-            stg16f(ps + c, make_float4(sg_s[j][0].x, sg_s[j][0].y, sg_s[j][1].x, sg_s[j][1].y));
-            stg16f(ps + c + 4, make_float4(sg_s[j][2].x, sg_s[j][2].y, sg_s[j][3].x, sg_s[j][3].y));
-            stg16f(pk + c, make_float4(kp_s[j][0].x, kp_s[j][0].y, kp_s[j][1].x, kp_s[j][1].y));
-            stg16f(pk + c + 4, make_float4(kp_s[j][2].x, kp_s[j][2].y, kp_s[j][3].x, kp_s[j][3].y));
-            stg16f(ps + D + c, make_float4(sg_h[j][0].x, sg_h[j][0].y, sg_h[j][1].x, sg_h[j][1].y));
-            stg16f(ps + D + c + 4, make_float4(sg_h[j][2].x, sg_h[j][2].y, sg_h[j][3].x, sg_h[j][3].y));
-            stg16f(pk + D + c, make_float4(kp_h[j][0].x, kp_h[j][0].y, kp_h[j][1].x, kp_h[j][1].y));
-            stg16f(pk + D + c + 4, make_float4(kp_h[j][2].x, kp_h[j][2].y, kp_h[j][3].x, kp_h[j][3].y));
+            stg16f(ps + c, make_float4(px_lo(sg_s[j][0]), px_hi(sg_s[j][0]), px_lo(sg_s[j][1]), px_hi(sg_s[j][1])));
+            stg16f(ps + c + 4, make_float4(px_lo(sg_s[j][2]), px_hi(sg_s[j][2]), px_lo(sg_s[j][3]), px_hi(sg_s[j][3])));
+            stg16f(pk + c, make_float4(px_lo(kp_s[j][0]), px_hi(kp_s[j][0]), px_lo(kp_s[j][1]), px_hi(kp_s[j][1])));
+            stg16f(pk + c + 4, make_float4(px_lo(kp_s[j][2]), px_hi(kp_s[j][2]), px_lo(kp_s[j][3]), px_hi(kp_s[j][3])));
+            stg16f(ps + D + c, make_float4(px_lo(sg_h[j][0]), px_hi(sg_h[j][0]), px_lo(sg_h[j][1]), px_hi(sg_h[j][1])));
+            stg16f(ps + D + c + 4,
+                   make_float4(px_lo(sg_h[j][2]), px_hi(sg_h[j][2]), px_lo(sg_h[j][3]), px_hi(sg_h[j][3])));
+            stg16f(pk + D + c, make_float4(px_lo(kp_h[j][0]), px_hi(kp_h[j][0]), px_lo(kp_h[j][1]), px_hi(kp_h[j][1])));
+            stg16f(pk + D + c + 4,
+                   make_float4(px_lo(kp_h[j][2]), px_hi(kp_h[j][2]), px_lo(kp_h[j][3]), px_hi(kp_h[j][3])));
         }
     }
 }
@@ -800,54 +858,62 @@ tree_level0_kernel(const float *__restrict__ in, float *__restrict__ ws_sig, flo
 
 // ==========================================================================
 // Tree fold: levels >= 1 and the final add.  One CTA per (sample, 32 columns);
-// lane = column.  Warp w folds level-1 groups w, w + W, ... from the level-0
-// partials in global memory; higher levels fold in shared memory.
+// lane = column.  Warp w folds the level-1 groups w, w + W, ... straight from
+// the level-0 nodes in global memory, all 32 children of a group requested at
+// once (one round trip); higher levels fold in shared memory.
 // ==========================================================================
-struct FoldSmem {
-    float s1[kMaxLevel1][32], k1[kMaxLevel1][32];
-    float s2[kMaxLevel1 / kTile][32], k2[kMaxLevel1 / kTile][32];
-};
-
-// one group of the fold: Neumaier sum of the children's sums in ascending
-// order (compensation c), children's corrections added in ascending order;
-// node = (sum, c + corrections).  Children are loaded eight at a time, the next
-// eight in flight while the current ones are added.
-__device__ __forceinline__ void fold_load8(const float *sig, const float *kap, size_t stride, int i0, int count,
-                                           float (&vs)[8], float (&vk)[8]) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-        if (i0 + q < count) {
-            vs[q] = sig[(size_t)(i0 + q) * stride];
-            vk[q] = kap[(size_t)(i0 + q) * stride];
-        }
+// shared memory of the fold: level-1 nodes s1, k1 [n1][32], then level-2
+// nodes s2, k2 [ceil(n1/32)][32] (n1 = ceil(T/32) <= 256)
+__host__ __device__ constexpr size_t fold_smem_bytes(int n1) {
+    return n1 <= 1 ? 0 : (size_t)2 * 32 * sizeof(float) * (n1 + (n1 + kTile - 1) / kTile);
 }
-__device__ __forceinline__ void fold_add8(const float (&vs)[8], const float (&vk)[8], int i0, int count, float &s,
-                                          float &c, float &k) {
+
+// One group: Neumaier sum of the children's sums in ascending order
+// (compensation c), the children's corrections added in ascending order;
+// node = (sum, c + corrections).
+__device__ __forceinline__ void fold_values(const float (&vs)[kTile], const float (&vk)[kTile], int count,
+                                            float &out_s, float &out_k) {
+    float s = vs[0], k = vk[0], c = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        if (i0 + q == 0) {
-            s = vs[0];
-            k = vk[0];
-        } else if (i0 + q < count) {
+    for (int q = 1; q < kTile; ++q) {
+        if (q < count) {
             twosum(s, c, vs[q]);
             k = __fadd_rn(k, vk[q]);
         }
     }
-}
-__device__ __forceinline__ void fold_group(const float *sig, const float *kap, size_t stride, int count,
-                                           float &out_s, float &out_k) {
-    float s = 0.0f, c = 0.0f, k = 0.0f;
-    float as[8], ak[8], bs[8], bk[8];
-    fold_load8(sig, kap, stride, 0, count, as, ak);
-    if (8 < count) fold_load8(sig, kap, stride, 8, count, bs, bk);
-    for (int i0 = 0; i0 < count; i0 += 16) {
-        fold_add8(as, ak, i0, count, s, c, k);
-        if (i0 + 16 < count) fold_load8(sig, kap, stride, i0 + 16, count, as, ak);
-        if (i0 + 8 < count) fold_add8(bs, bk, i0 + 8, count, s, c, k);
-        if (i0 + 24 < count) fold_load8(sig, kap, stride, i0 + 24, count, bs, bk);
-    }
     out_s = s;
     out_k = __fadd_rn(c, k);
+}
+
+__device__ __forceinline__ void fold_group(const float *sig, const float *kap, size_t stride, int count,
+                                           float &out_s, float &out_k) {
+    float vs[kTile], vk[kTile];
+    if (count == kTile) {
+        // a full group: all 64 loads issued before the first add
+#pragma unroll
+        for (int q = 0; q < kTile; ++q) vs[q] = __ldcg(sig + (size_t)q * stride);
+#pragma unroll
+        for (int q = 0; q < kTile; ++q) vk[q] = __ldcg(kap + (size_t)q * stride);
+    } else {
+#pragma unroll
+        for (int q = 0; q < kTile; ++q) {
+            vs[q] = q < count ? __ldcg(sig + (size_t)q * stride) : 0.0f;
+            vk[q] = q < count ? __ldcg(kap + (size_t)q * stride) : 0.0f;
+        }
+    }
+    fold_values(vs, vk, count, out_s, out_k);
+}
+
+// the same over shared memory (levels >= 2)
+__device__ __forceinline__ void fold_group_smem(const float *sig, const float *kap, int count, float &out_s,
+                                                float &out_k) {
+    float vs[kTile], vk[kTile];
+#pragma unroll
+    for (int q = 0; q < kTile; ++q) {
+        vs[q] = q < count ? sig[q * 32] : 0.0f;
+        vk[q] = q < count ? kap[q * 32] : 0.0f;
+    }
+    fold_values(vs, vk, count, out_s, out_k);
 }
 
 constexpr int kFoldWarps = 8;
@@ -855,8 +921,7 @@ constexpr int kFoldWarps = 8;
 __global__ void __launch_bounds__(kFoldWarps * 32)
 tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_kap, float *__restrict__ out,
                  int T, int H) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    FoldSmem &sm = *reinterpret_cast<FoldSmem *>(smem_raw);
+    extern __shared__ __align__(128) float fold_sh[];
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -872,13 +937,23 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
         return;
     }
     const int n1 = (T + kTile - 1) / kTile;
+    const int m2 = (n1 + kTile - 1) / kTile;
+    float(*s1)[32] = reinterpret_cast<float(*)[32]>(fold_sh);
+    float(*k1)[32] = s1 + n1;
+    float(*s2)[32] = k1 + n1;
+    float(*k2)[32] = s2 + m2;
     for (int gi = warp; gi < n1; gi += W) {
         const int i0 = gi * kTile;
         const int cnt = min(kTile, T - i0);
         float s, k;
         fold_group(ws_sig + base + (size_t)i0 * H, ws_kap + base + (size_t)i0 * H, (size_t)H, cnt, s, k);
-        sm.s1[gi][lane] = s;
-        sm.k1[gi][lane] = k;
+        if (n1 == 1) {  // the level-1 node is the root
+            if (live) out[(size_t)b * H + col] = __fadd_rn(s, k);
+            pdl_trigger();
+            return;
+        }
+        s1[gi][lane] = s;
+        k1[gi][lane] = k;
     }
     __syncthreads();
     // levels >= 2, alternating between the two shared buffers
@@ -891,13 +966,13 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
             const int cnt = min(kTile, nn - i0);
             float s, k;
             if (in_first) {
-                fold_group(&sm.s1[i0][lane], &sm.k1[i0][lane], 32, cnt, s, k);
-                sm.s2[gi][lane] = s;
-                sm.k2[gi][lane] = k;
+                fold_group_smem(&s1[i0][lane], &k1[i0][lane], cnt, s, k);
+                s2[gi][lane] = s;
+                k2[gi][lane] = k;
             } else {
-                fold_group(&sm.s2[i0][lane], &sm.k2[i0][lane], 32, cnt, s, k);
-                sm.s1[gi][lane] = s;
-                sm.k1[gi][lane] = k;
+                fold_group_smem(&s2[i0][lane], &k2[i0][lane], cnt, s, k);
+                s1[gi][lane] = s;
+                k1[gi][lane] = k;
             }
         }
         __syncthreads();
@@ -906,8 +981,8 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
     }
     pdl_trigger();
     if (warp == 0 && live) {
-        const float s = in_first ? sm.s1[0][lane] : sm.s2[0][lane];
-        const float k = in_first ? sm.k1[0][lane] : sm.k2[0][lane];
+        const float s = in_first ? s1[0][lane] : s2[0][lane];
+        const float k = in_first ? k1[0][lane] : k2[0][lane];
         out[(size_t)b * H + col] = __fadd_rn(s, k);
     }
 }
@@ -926,7 +1001,7 @@ static cudaError_t launch_fold(const float *sig, const float *kap, float *out, i
                                cudaStream_t stream, const DeviceInfo &dev) {
     const int n1 = (T + kTile - 1) / kTile;
     const int warps = T == 1 ? 1 : min(kFoldWarps, n1);
-    const size_t smem = sizeof(FoldSmem);
+    const size_t smem = fold_smem_bytes(n1);
     cudaError_t err = ensure_smem_attr((const void *)tree_fold_kernel, smem, dev);
     if (err != cudaSuccess) return err;
     return launch_pdl(tree_fold_kernel, dim3((H + 31) / 32, B), dim3(32 * warps), smem, stream,
@@ -942,20 +1017,22 @@ template <int VPT, int MAXNT, int MINB, int RB, int NST>
 static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                                     const float *rstd, uint16_t *dx, float *sig, float *kap, int B, int S, int D,
                                     int T, cudaStream_t stream, const DeviceInfo &dev) {
-    static_assert(NST == 2 * RB && RB <= kRowBlock, "two blocks of rows in flight");
     const int V = D / 8;
     const int nt = ((V + VPT - 1) / VPT + 31) / 32 * 32;
     const size_t smem = ((sizeof(BwdSmem) + 127) / 128) * 128 + (size_t)NST * 4 * D;
-    auto kern = out_bwd_tile_kernel<VPT, MAXNT, MINB, RB, NST>;
+    // every thread's vectors inside the row: the form without bounds tests
+    auto kern = nt * VPT == V ? out_bwd_tile_kernel<VPT, MAXNT, MINB, RB, NST, true>
+                              : out_bwd_tile_kernel<VPT, MAXNT, MINB, RB, NST, false>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(T, B), dim3(nt), smem, stream, dy, x, emb, mean, rstd, dx, sig, kap,
                       S, D, T);
 }
 
-// Stages of up to 12 KB (D <= 3072): two CTAs of <= 384 threads per SM, blocks
-// of 4 rows, 8 stages; up to 16 KB: one CTA per SM, the same ring; longer
-// rows: blocks of 2 rows and 4 stages (at most 128 KB of stages).
+// 16 columns per thread.  Stages of up to 12 KB (D <= 3072): two CTAs of <= 192
+// threads per SM, blocks of 4 rows, 8 stages; up to 16 KB: one CTA of <= 256
+// threads per SM, the same ring; longer rows: 32 columns per thread, blocks of
+// 2 rows and 4 stages (at most 128 KB).
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
                            cudaStream_t stream, const DeviceInfo &dev) {
@@ -967,11 +1044,11 @@ cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t
     const int V = D / 8;
     cudaError_t err;
     if (V <= 384)
-        err = launch_out_bwd_t<1, 384, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<2, 192, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     else if (V <= 512)
-        err = launch_out_bwd_t<1, 512, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<2, 256, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     else
-        err = launch_out_bwd_t<2, 512, 1, 2, 4>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<4, 256, 1, 2, 4>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
 }
