@@ -318,6 +318,52 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// --------------------------------------------------------------------------
+// L2 eviction priority.  A step streams its token tensors (x, dy, out, dx:
+// hundreds of MB, each read or written once per call) past the weights W
+// (37.7 MB at D = 3072), which both projections read.  Streams are marked
+// evict-first and W evict-last, so that W read by the forward projection can
+// still be in L2 when the backward projection reads it.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 16-byte read-only global load with an L2 policy
+__device__ __forceinline__ uint4 ldg16_hint(const void *p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+// 16-byte global store with an L2 policy
+__device__ __forceinline__ void stg16_hint(void *p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+// bulk copy global -> shared with an L2 policy (as bulk_g2s)
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+// L2 prefetch with a policy (as bulk_prefetch_l2)
+__device__ __forceinline__ void bulk_prefetch_l2_hint(const void *src, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+
 // Ask the memory system to bring [src, src + bytes) into L2 (no completion
 // to wait for).  L2 is the point of coherence, so this is safe even while the
 // preceding kernel may still write the range: later reads see its writes.

@@ -101,6 +101,7 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
     float2 onep[VPT][4], shift[VPT][4];  // modulation parameters of the current sample, by column pair
     long long cur_b = -1;
     const float Df = (float)D;
+    const uint64_t pol_out = l2_evict_first();  // out is not read again by this operator
 
     for (int r0 = 0; r0 < nrows; r0 += BLK) {
         const int nb = min(BLK, nrows - r0);
@@ -223,7 +224,7 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
                         const float2 m = f2add(pr, shift[j][q]);
                         o[q] = pack_bf16x2(m.x, m.y);
                     }
-                    stg16(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
+                    stg16_hint(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_out);
                 }
             }
             if (t == 0) {
@@ -329,6 +330,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     pdl_trigger();
 
     const float Df = (float)D;
+    const uint64_t pol_out = l2_evict_first();  // out is not read again by this operator
     for (int k = 0; k < nrows; ++k) {
         const size_t r = row0 + (size_t)k * NW;
         const int st = k % NS;
@@ -407,7 +409,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
                     const float2 m = f2add(pr, shf[q]);
                     o[q] = pack_bf16x2(m.x, m.y);
                 }
-                stg16(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
+                stg16_hint(orow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_out);
             }
         }
         if (lane == 0) {
@@ -599,12 +601,14 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         const int v = tid + NT * j;
         sc_v[j] = (EXACT || v < V) ? ldg16(e + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
+    // dy and dx are streamed once: evict-first in L2
+    const uint64_t pol_stream = l2_evict_first();
     if (tid == 0) {
         for (int i = 0; i < NST && i < n; ++i) {
             unsigned char *dst = stages + (size_t)i * stage_bytes;
             mbar_arrive_expect_tx(&sm.full[i], stage_bytes);
             bulk_g2s(dst, x + (row0 + i) * D, row_bytes, &sm.full[i]);
-            bulk_g2s(dst + row_bytes, dy + (row0 + i) * D, row_bytes, &sm.full[i]);
+            bulk_g2s_hint(dst + row_bytes, dy + (row0 + i) * D, row_bytes, &sm.full[i], pol_stream);
             sm.last[i] = i;
         }
     }
@@ -689,7 +693,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                     const px2 t = px_fma(px_bf16(xa[q]), nk2, k3v);
                     o[q] = px_to_bf16x2(px_fma(gh, rs2, t));
                 }
-                stg16(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]));
+                stg16_hint(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_stream);
             }
         }
     };
@@ -777,7 +781,8 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                         unsigned char *dst = stages + (size_t)st * stage_bytes;
                         mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
                         bulk_g2s(dst, x + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
-                        bulk_g2s(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st]);
+                        bulk_g2s_hint(dst + row_bytes, dy + (row0 + i + NST) * D, row_bytes, &sm.full[st],
+                                      pol_stream);
                         sm.last[st] = i + NST;
                     }
                 }
@@ -923,6 +928,7 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
                  int T, int H) {
     extern __shared__ __align__(128) float fold_sh[];
     pdl_wait();
+    pdl_trigger();  // the next kernel may become resident and wait; it reads out only after its own wait
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
@@ -933,7 +939,6 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
 
     if (T == 1) {  // the tile is the root
         if (warp == 0 && live) out[(size_t)b * H + col] = __fadd_rn(ws_sig[base], ws_kap[base]);
-        pdl_trigger();
         return;
     }
     const int n1 = (T + kTile - 1) / kTile;
@@ -949,7 +954,6 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
         fold_group(ws_sig + base + (size_t)i0 * H, ws_kap + base + (size_t)i0 * H, (size_t)H, cnt, s, k);
         if (n1 == 1) {  // the level-1 node is the root
             if (live) out[(size_t)b * H + col] = __fadd_rn(s, k);
-            pdl_trigger();
             return;
         }
         s1[gi][lane] = s;
@@ -979,7 +983,6 @@ tree_fold_kernel(const float *__restrict__ ws_sig, const float *__restrict__ ws_
         in_first = !in_first;
         nn = m;
     }
-    pdl_trigger();
     if (warp == 0 && live) {
         const float s = in_first ? s1[0][lane] : s2[0][lane];
         const float k = in_first ? k1[0][lane] : k2[0][lane];

@@ -88,10 +88,11 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
     // W and bias are inputs of this call, never outputs of the kernel that
     // precedes this one (the SiLU kernel above), so they are read before the wait.
     uint4 wv[kFwdVL];
+    const uint64_t pol_w = l2_evict_last();  // the backward projection reads W again
 #pragma unroll
     for (int q = 0; q < kFwdVL; ++q) {
         const int v = lane + 32 * q;
-        if (v < V) wv[q] = ldg16(wrow + (size_t)v * 8);
+        if (v < V) wv[q] = ldg16_hint(wrow + (size_t)v * 8, pol_w);
     }
     const float bn = bf16f(bias[live ? n : N - 1]);
     pdl_wait();
@@ -108,7 +109,7 @@ proj_fwd_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ bia
 #pragma unroll
                 for (int q = 0; q < kFwdVL; ++q) {
                     const int v = v0 + lane + 32 * q;
-                    if (v < V) wv[q] = ldg16(wrow + (size_t)v * 8);
+                    if (v < V) wv[q] = ldg16_hint(wrow + (size_t)v * 8, pol_w);
                 }
             }
 #pragma unroll
@@ -169,11 +170,12 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ u, const uint16_t *__restric
     const int nrows = gw < N ? (N - 1 - gw) / NW + 1 : 0;  // rows of this warp
 
     uint4 wa[kStreamVL], wb[kStreamVL];
+    const uint64_t pol_w = l2_evict_last();  // the backward projection reads W again
     auto load_row = [&](uint4(&w)[kStreamVL], int n) {
 #pragma unroll
         for (int j = 0; j < kStreamVL; ++j) {
             const int v = lane + 32 * j;
-            w[j] = v < V ? ldg16(W + (size_t)n * D + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
+            w[j] = v < V ? ldg16_hint(W + (size_t)n * D + (size_t)v * 8, pol_w) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
     constexpr int R = BC <= 2 ? 2 : 1;  // rows in flight per warp (registers)
@@ -300,7 +302,15 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                          kchunk == 0 && lane == 0;
     constexpr int kPre = BC <= 2 ? kPreMax : kPreMax / 2;  // fewer rows in flight where more samples need registers
 
+    // W is an input of this call: its rows of this CTA are brought into L2
+    // while the preceding kernel finishes (L2 is the point of coherence, so
+    // reads after the wait still see any write of the preceding kernel)
+    if (B > 0 && threadIdx.x < kSlabRows && n0 + (int)threadIdx.x < N && kchunk * kProjKChunk < D)
+        bulk_prefetch_l2(W + (size_t)(n0 + threadIdx.x) * D + (size_t)kchunk * kProjKChunk,
+                         (uint32_t)min(kProjKChunk, D - kchunk * kProjKChunk) * 2u);
     pdl_wait();
+    pdl_trigger();  // the next kernel may become resident and wait for this one
+    const uint64_t pol_dw = l2_evict_first();  // dW is written once
 
     for (int b0 = 0; b0 < B || (WITH_W && b0 == 0); b0 += BC) {
         const int nb = max(0, min(BC, B - b0));
@@ -379,9 +389,10 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                             stg16f(pa + 4, make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y));
                         }
                         if (WM == kSlabDwOut || dW)
-                            stg16(dW + (size_t)n * D + col,
-                                  make_uint4(pack_bf16x2(acc[0].x, acc[0].y), pack_bf16x2(acc[1].x, acc[1].y),
-                                             pack_bf16x2(acc[2].x, acc[2].y), pack_bf16x2(acc[3].x, acc[3].y)));
+                            stg16_hint(dW + (size_t)n * D + col,
+                                       make_uint4(pack_bf16x2(acc[0].x, acc[0].y), pack_bf16x2(acc[1].x, acc[1].y),
+                                                  pack_bf16x2(acc[2].x, acc[2].y), pack_bf16x2(acc[3].x, acc[3].y)),
+                                       pol_dw);
                     }
                 }
                 if (WITH_W && want_db && i < cnt) {
@@ -422,7 +433,6 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
         }
         __syncthreads();
     }
-    pdl_trigger();
 }
 
 // --------------------------------------------------------------------------
@@ -434,6 +444,7 @@ __global__ void __launch_bounds__(256)
 proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__ temb, uint16_t *__restrict__ d_temb,
                       int B, int D, int nslab) {
     pdl_wait();
+    pdl_trigger();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
     if (i < BD) {
@@ -447,7 +458,6 @@ proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__
             if (s < nslab) tot = __fadd_rn(tot, part[s]);
         d_temb[i] = bf16_bits(__fmul_rn(tot, dsilu_f32(bf16f(temb[i]))));
     }
-    pdl_trigger();
 }
 
 // --------------------------------------------------------------------------
