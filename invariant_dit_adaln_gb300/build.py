@@ -41,22 +41,27 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str | None = None) -> str:
+    """Compile and link the library; returns its path.  `variant` names a test
+    build with extra flags, linked to lib/<variant>/libadaln.so with objects in
+    _build/<variant>/ (the release library is lib/libadaln.so)."""
+    lib = LIB if variant is None else os.path.join(LIBDIR, variant, "libadaln.so")
+    objdir = BUILD if variant is None else os.path.join(BUILD, variant)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,13 +73,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     logs = "".join(log for _, log in results)
     if verbose and logs.strip():
         print(logs, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+# Test build: the first wait of every waiting kernel goes to an mbarrier that
+# nothing arrives on, with a 200 us limit (the kernels' time-out path).
+WAIT_TEST_FLAGS = ["-DADALN_TEST_WAIT_NEVER_NS=200000"]
 
 
 if __name__ == "__main__":

@@ -101,6 +101,23 @@ size_t tiles(int S) { return (size_t)((S + kTile - 1) / kTile); }
 
 }  // namespace
 
+adaln_status check_current_device(DeviceInfo *info) { return current_device(info); }
+
+adaln_status check_out_bwd_args(const void *dy, const void *x, const void *emb, const float *mean, const float *rstd,
+                                const void *dx, const float *d_emb, int B, int S, int D) {
+    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    const size_t rows = (size_t)B * S;
+    const Buf ins[] = {{dy, rows * D * 2}, {x, rows * D * 2}, {emb, (size_t)B * 2 * D * 2}, {mean, rows * 4},
+                       {rstd, rows * 4}};
+    const Buf outs[] = {{dx, rows * D * 2}, {d_emb, (size_t)B * 2 * D * 4}};
+    if (any_missing(ins, 5) || any_missing(outs, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(emb) || !aligned16(mean) || !aligned16(rstd) ||
+        !aligned16(dx) || !aligned16(d_emb))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 2, ins, 5)) return ADALN_ERR_ALIAS;
+    return ADALN_OK;
+}
+
 cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &dev) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     static std::unordered_map<const void *, size_t> done[64];
@@ -196,17 +213,15 @@ adaln_status adaln_out_fwd(const adaln_bf16 *x, const adaln_bf16 *emb, adaln_bf1
 adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb, const float *mean,
                            const float *rstd, adaln_bf16 *dx, float *d_emb, void *workspace, size_t workspace_bytes,
                            int B, int S, int D, void *stream) {
-    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    adaln_status chk = check_out_bwd_args(dy, x, emb, mean, rstd, dx, d_emb, B, S, D);
+    if (chk == ADALN_ERR_SHAPE || chk == ADALN_ERR_NULL) return chk;
     const size_t rows = (size_t)B * S;
     const size_t need = adaln_out_bwd_workspace_bytes(B, S, D);
+    if (chk == ADALN_ERR_ALIGN || !aligned16(workspace)) return ADALN_ERR_ALIGN;
     const Buf ins[] = {{dy, rows * D * 2}, {x, rows * D * 2}, {emb, (size_t)B * 2 * D * 2}, {mean, rows * 4},
                        {rstd, rows * 4}};
     const Buf outs[] = {{dx, rows * D * 2}, {d_emb, (size_t)B * 2 * D * 4}, {workspace, need}};
-    if (any_missing(ins, 5) || any_missing(outs, 2)) return ADALN_ERR_NULL;
-    if (!aligned16(dy) || !aligned16(x) || !aligned16(emb) || !aligned16(mean) || !aligned16(rstd) ||
-        !aligned16(dx) || !aligned16(d_emb) || !aligned16(workspace))
-        return ADALN_ERR_ALIGN;
-    if (any_alias(outs, 3, ins, 5)) return ADALN_ERR_ALIAS;
+    if (chk == ADALN_ERR_ALIAS || any_alias(outs, 3, ins, 5)) return ADALN_ERR_ALIAS;
     if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
     DeviceInfo dev;
     adaln_status st = current_device(&dev);

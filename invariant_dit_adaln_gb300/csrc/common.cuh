@@ -27,6 +27,7 @@ enum DeviceError : unsigned {
     kErrNone = 0,
     kErrOutFwdWait = 0x101,
     kErrOutBwdWait = 0x201,
+    kErrDrainFailed = 0x8000,  // or-ed in: an issued copy did not land while leaving
 };
 
 // --------------------------------------------------------------------------

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "adaln.h"
+
 namespace adaln {
 
 struct DeviceInfo {
@@ -14,6 +16,14 @@ struct DeviceInfo {
     int cc_major;
     int cc_minor;
 };
+
+// api.cu: checks of the C ABI.  check_current_device: the current device and
+// its properties; ADALN_ERR_DEVICE unless it is compute capability 10.3.
+// check_out_bwd_args: the checks of adaln_out_bwd on its tensor arguments
+// (sizes, NULL pointers, alignment, overlaps), the workspace excluded.
+adaln_status check_current_device(DeviceInfo *info);
+adaln_status check_out_bwd_args(const void *dy, const void *x, const void *emb, const float *mean, const float *rstd,
+                                const void *dx, const float *d_emb, int B, int S, int D);
 
 // Raise the dynamic shared-memory limit of a kernel once per (kernel, device).
 cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &dev);

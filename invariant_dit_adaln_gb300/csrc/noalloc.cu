@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "adaln.h"
+#include "internal.h"
 
 namespace adaln {
 
@@ -30,15 +31,11 @@ namespace {
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[64];  // device address of the array, per device, once looked up
 
-// The array's device address for the current device.  In host code the name
-// g_noalloc_scratch is only a host-side stand-in, never a device address, so
-// the address is asked from the runtime, with the device current.
-adaln_status noalloc_scratch(void **ptr) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return ADALN_ERR_DEVICE;
-    }
+// The array's device address on the current device `dev`.  In host code the
+// name g_noalloc_scratch is only a host-side stand-in, never a device address,
+// so the address is asked from the runtime, with the device current.
+adaln_status noalloc_scratch(int dev, void **ptr) {
+    if (dev < 0 || dev >= 64) return ADALN_ERR_DEVICE;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_ptr[dev] == nullptr) {
         void *p = nullptr;
@@ -60,16 +57,24 @@ extern "C" {
 adaln_status adaln_out_bwd_noalloc(const adaln_bf16 *dy, const adaln_bf16 *x, const adaln_bf16 *emb,
                                    const float *mean, const float *rstd, adaln_bf16 *dx, float *d_emb, int B, int S,
                                    int D, void *stream) {
-    // sizes first: the partials must fit in the library's own array
-    if (D < 8 || D > 8192 || D % 8 != 0 || B < 0 || S < 0 || S > 262144 || B > 65535) return ADALN_ERR_SHAPE;
-    if (adaln_out_bwd_workspace_bytes(B, S, D) > adaln::kNoAllocScratchBytes) return ADALN_ERR_SHAPE;
+    using namespace adaln;
+    // the checks of adaln_out_bwd, in its order: sizes (here also: the partials
+    // must fit in the library's array), NULL pointers, alignment, overlaps,
+    // then the device; only then the array's address
+    adaln_status st = check_out_bwd_args(dy, x, emb, mean, rstd, dx, d_emb, B, S, D);
+    if (st == ADALN_ERR_SHAPE) return st;
+    if (adaln_out_bwd_workspace_bytes(B, S, D) > kNoAllocScratchBytes) return ADALN_ERR_SHAPE;
+    if (st != ADALN_OK) return st;
+    DeviceInfo dev;
+    st = check_current_device(&dev);
+    if (st != ADALN_OK) return st;
     void *scratch = nullptr;
     if (adaln_out_bwd_workspace_bytes(B, S, D) > 0) {
-        adaln_status st = adaln::noalloc_scratch(&scratch);
+        st = noalloc_scratch(dev.device, &scratch);
         if (st != ADALN_OK) return st;
     }
-    // the same checks and kernels as adaln_out_bwd, with the array as workspace
-    return adaln_out_bwd(dy, x, emb, mean, rstd, dx, d_emb, scratch, adaln::kNoAllocScratchBytes, B, S, D, stream);
+    // the same kernels as adaln_out_bwd, with the array as workspace
+    return adaln_out_bwd(dy, x, emb, mean, rstd, dx, d_emb, scratch, kNoAllocScratchBytes, B, S, D, stream);
 }
 
 }  // extern "C"

@@ -20,6 +20,26 @@ namespace adaln {
 static __device__ unsigned g_err;  // device-side error word (see adaln_device_error)
 
 __device__ __forceinline__ void report_error(unsigned code) { atomicCAS(&g_err, 0u, code); }
+// a copy that did not land within the drain's limit while a kernel was leaving
+// after an error: marked by a bit of its own next to the first error code
+__device__ __forceinline__ void report_drain_failure() { atomicOr(&g_err, kErrDrainFailed); }
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    if (!mbar_wait_bounded(bar, parity, 10000000ull)) report_drain_failure();
+}
+
+// Test builds only (ADALN_TEST_WAIT_NEVER_NS defined): the first wait of each
+// waiting warp goes to an mbarrier that nothing ever arrives on, with that
+// limit in nanoseconds, so the time-out path (error word, drain of the issued
+// copies, early return) runs on the GPU without any fault or hang.  Release
+// builds compile none of it.
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+#define ADALN_NEVER_BAR uint64_t never;
+__device__ __forceinline__ bool test_wait_never(uint64_t *never) {
+    return mbar_wait_bounded(never, 0u, (uint64_t)(ADALN_TEST_WAIT_NEVER_NS));
+}
+#else
+#define ADALN_NEVER_BAR
+#endif
 
 // ==========================================================================
 // Forward: one warp-group (128 threads) per token row, persistent.
@@ -44,6 +64,7 @@ struct FwdSmem {
     float red[kWG][2][kFwdBlock][4];  // [warp-group][sum, squares][row of block][warp]
     float mu[kWG][kFwdBlock], rs[kWG][kFwdBlock];
     uint64_t full[kWG][2 * kFwdBlock];
+    ADALN_NEVER_BAR
 };
 
 // barrier of one warp-group, and a vote: is `flag` set in any of its threads?
@@ -84,6 +105,9 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
 
     if (t == 0) {
         for (int s = 0; s < NST; ++s) mbar_init(&sm.full[wg][s], 1);
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        if (wg == 0) mbar_init(&sm.never, 1);
+#endif
         fence_barrier_init();
         // warm L2 with the first rows while the preceding kernel finishes
         for (int i = 0; i < NST && i < nrows; ++i) bulk_prefetch_l2(x + (size_t)(r_begin + i) * D, row_bytes);
@@ -111,6 +135,9 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
         for (int jr = 0; jr < BLK; ++jr) if (jr < nb) {
             const int i = r0 + jr;
             const int st = i % NST;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+            if (i == 0) ok = test_wait_never(&sm.never) && ok;
+#endif
             ok = mbar_wait_bounded(&sm.full[wg][st], (uint32_t)(i / NST) & 1u) && ok;
             const unsigned char *row = my_stages + (size_t)st * row_bytes;
             float2 s1 = make_float2(0.0f, 0.0f);
@@ -133,8 +160,7 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
                 report_error(kErrOutFwdWait);
                 // let the copies this warp-group issued finish before leaving
                 const int issued = min(nrows, r0 + NST);
-                for (int k = r0; k < issued; ++k)
-                    mbar_wait_bounded(&sm.full[wg][k % NST], (uint32_t)(k / NST) & 1u, 10000000ull);
+                for (int k = r0; k < issued; ++k) drain_wait(&sm.full[wg][k % NST], (uint32_t)(k / NST) & 1u);
             }
             return;
         }
@@ -270,7 +296,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     const int NW = blockDim.x >> 5;
     const int V = D >> 3;
     const int row_bytes = D * 2;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);             // [warps][NS]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);             // [warps][NS] (+ 1: test builds)
     float *t_onep = reinterpret_cast<float *>(smem_raw + 1024);          // [D]
     float *t_shift = t_onep + D;                                         // [D]
     unsigned char *ring = smem_raw + 1024 + (size_t)D * 8;               // [warps][NS][row]
@@ -286,6 +312,9 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&my_full[s], 1);
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        mbar_init(&full[MAXW * NS + warp], 1);  // this warp's never-completing barrier
+#endif
         fence_barrier_init();
     }
     __syncwarp();
@@ -334,14 +363,18 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     for (int k = 0; k < nrows; ++k) {
         const size_t r = row0 + (size_t)k * NW;
         const int st = k % NS;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        const bool ok = (k == 0 ? test_wait_never(&full[MAXW * NS + warp]) : true) &&
+                        mbar_wait_bounded(&my_full[st], (uint32_t)(k / NS) & 1u);
+#else
         const bool ok = mbar_wait_bounded(&my_full[st], (uint32_t)(k / NS) & 1u);
+#endif
         if (__any_sync(0xFFFFFFFFu, !ok)) {
             if (lane == 0) {
                 report_error(kErrOutFwdWait);
                 // let the copies this warp issued finish before leaving
                 const int issued = min(nrows, k + NS);
-                for (int q = k; q < issued; ++q)
-                    mbar_wait_bounded(&my_full[q % NS], (uint32_t)(q / NS) & 1u, 10000000ull);
+                for (int q = k; q < issued; ++q) drain_wait(&my_full[q % NS], (uint32_t)(q / NS) & 1u);
             }
             return;
         }
@@ -515,6 +548,7 @@ struct BwdSmem {
     unsigned rel[kBwdMaxStages];    // warps done with the rows of a block of stages
     int last[kBwdMaxStages];        // latest row copied into a stage (-1: none)
     int abort;                      // a wait ran out of time
+    ADALN_NEVER_BAR
 };
 
 // The NV partial sums of a warp's lanes reduced at once (a transposed
@@ -581,6 +615,9 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             sm.last[s] = -1;
         }
         sm.abort = 0;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        mbar_init(&sm.never, 1);
+#endif
         fence_barrier_init();
     }
     __syncthreads();
@@ -705,6 +742,9 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         const int nb = min(RB, n - r0);
         // ---- phase 1: tree products and the row sums ----
         bool landed = true;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        if (blk == 0) landed = test_wait_never(&sm.never);
+#endif
 #pragma unroll
         for (int jr = 0; jr < RB; ++jr)
             if (jr < nb)
@@ -795,8 +835,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
             report_error(kErrOutBwdWait);
             // let the copies this CTA issued land before it leaves
             for (int st = 0; st < NST; ++st)
-                if (sm.last[st] >= 0)
-                    mbar_wait_bounded(&sm.full[st], (uint32_t)(sm.last[st] / NST) & 1u, 10000000ull);
+                if (sm.last[st] >= 0) drain_wait(&sm.full[st], (uint32_t)(sm.last[st] / NST) & 1u);
         }
         return;
     }

@@ -63,6 +63,7 @@ def _load():
             "oracle_proj_bwd": [P, P, P, P, P, P, I, I],
             "oracle_proj_bwd_f64": [P, P, P, P, P, P, I, I],
             "oracle_wgrad_seq_f32": [P, P, P, P, I, I, I],
+            "oracle_wgrad_seq_f32_rows": [P, P, P, I, P, P, I, I],
             "oracle_bf16_from_f64": [P, P, Lg],
         }
         for name, args in sig.items():
@@ -244,6 +245,19 @@ def wgrad_seq_f32(d_emb, temb, dW_acc=None, db_acc=None, accumulate=False):
     dW = np.zeros((2 * D, D), np.float32) if dW_acc is None else np.array(dW_acc, dtype=np.float32, copy=True)
     db = np.zeros(2 * D, np.float32) if db_acc is None else np.array(db_acc, dtype=np.float32, copy=True)
     _load().oracle_wgrad_seq_f32(_p(d_emb), _p(temb), _p(dW), _p(db), int(bool(accumulate)), B, D)
+    return dW, db
+
+
+def wgrad_seq_f32_rows(d_emb, temb, rows):
+    """Rows `rows` of (dW_acc, db_acc) of wgrad_seq_f32 started from +0:
+    (dW fp32 [len(rows), D], db fp32 [len(rows)])."""
+    d_emb, temb = _c(d_emb, np.float32), _c(temb, np.uint16)
+    B, D = temb.shape
+    rows = _c(rows, np.int32)
+    assert rows.ndim == 1 and np.all((rows >= 0) & (rows < 2 * D))
+    dW = np.empty((len(rows), D), np.float32)
+    db = np.empty(len(rows), np.float32)
+    _load().oracle_wgrad_seq_f32_rows(_p(d_emb), _p(temb), _p(rows), len(rows), _p(dW), _p(db), B, D)
     return dW, db
 
 

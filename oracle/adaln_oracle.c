@@ -560,6 +560,30 @@ void oracle_wgrad_seq_f32(const float *d_emb, const uint16_t *temb, float *dW_ac
     free(e); free(u);
 }
 
+/* The same order for the listed output rows only (rows[0..nrows)), each from
+ * +0: dW_rows[i, k] = sum over b ascending of e[b, rows[i]] * u[b, k] in fp32,
+ * db_rows[i] likewise.  For checking a sample of rows of a large batch.      */
+void oracle_wgrad_seq_f32_rows(const float *d_emb, const uint16_t *temb, const int *rows, int nrows,
+                               float *dW_rows, float *db_rows, int B, int D)
+{
+    int N = 2 * D;
+    float *u = malloc(sizeof(float) * (size_t)B * D);
+    for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = bf16_to_f32(bf16_from_f64(silu64(bf16_to_f64(temb[i]))));
+    for (int r = 0; r < nrows; ++r) {
+        int n = rows[r];
+        float *dst = dW_rows + (size_t)r * D;
+        for (int k = 0; k < D; ++k) dst[k] = 0.0f;
+        float a = 0.0f;
+        for (int b = 0; b < B; ++b) {
+            float e = bf16_to_f32(bf16_from_f32(d_emb[(size_t)b * N + n]));
+            for (int k = 0; k < D; ++k) dst[k] = dst[k] + e * u[(size_t)b * D + k];
+            a = a + e;
+        }
+        db_rows[r] = a;
+    }
+    free(u);
+}
+
 /* ------------------------------------------------------------------------ */
 /* format helpers exported for the tests                                     */
 /* ------------------------------------------------------------------------ */

@@ -133,6 +133,24 @@ def test_out_bwd_checks(L, no_gpu):
     assert out_bwd(L, nws=L.adaln_out_bwd_workspace_bytes(2, 33, 3072) - 1) == WORKSPACE
 
 
+def out_bwd_noalloc(L, dy=0, x=1, emb=2, mean=3, rstd=4, dx=5, d_emb=6, B=2, S=33, D=3072):
+    p = [None if a is None else (fake(a) if isinstance(a, int) else a) for a in (dy, x, emb, mean, rstd, dx, d_emb)]
+    return L.adaln_out_bwd_noalloc(*p, B, S, D, None)
+
+
+def test_out_bwd_noalloc_checks(L, no_gpu):
+    """The checks of adaln_out_bwd in the same order, the array's size limit
+    counted with the sizes; the device is checked before the library's array
+    is looked up."""
+    assert out_bwd_noalloc(L, D=3004) == SHAPE
+    assert out_bwd_noalloc(L, S=8192 + 32) == SHAPE       # partials beyond the 24 MiB array
+    assert out_bwd_noalloc(L, dy=None, S=8192 + 32) == SHAPE
+    assert out_bwd_noalloc(L, dy=None) == NULL
+    assert out_bwd_noalloc(L, mean=fake(3, 4)) == ALIGN
+    assert out_bwd_noalloc(L, dx=fake(1)) == ALIAS
+    assert out_bwd_noalloc(L) == DEVICE                     # valid arguments: the device check comes next
+
+
 # --- token_sum_tree ---------------------------------------------------------
 
 def tree(L, inp=0, out=1, ws=2, nws=None, B=2, S=33, H=6144):

@@ -160,12 +160,49 @@ def test_chunking_invariance(n, chunks):
         assert torch.equal(gb.view(torch.int32), refb.view(torch.int32)), c
 
 
+def _oracle_check_samples(dev, ref, refW, refb, samples, rows, D):
+    """The 1 x n chunk against the oracle: every per-sample output of the
+    listed samples, and the listed rows of dW, db summed over all n samples
+    (the chunked projection and the tiled weight-gradient kernels run only at
+    batches this large)."""
+    import numpy as np
+    import oracle
+    from gpu_util import host_bf16, host_f32
+    from tolerance import (assert_bitwise, bf16_to_f64, check_bf16, check_f32, check_rows, floor_d_emb,
+                           floor_d_temb)
+    oracle.build()
+    idx = torch.tensor(samples, device="cuda")
+    h = {k: host_bf16(dev[k].index_select(0, idx)) for k in ("x", "dy", "temb")}
+    W, b = host_bf16(dev["W"]), host_bf16(dev["b"])
+    g = {k: (host_bf16(v.index_select(0, idx)) if v.dtype == torch.bfloat16 else host_f32(v.index_select(0, idx)))
+         for k, v in ref.items()}
+    check_bf16(g["emb"], oracle.proj_fwd(h["temb"], W, b), what="1x4096 chunk: emb of sampled samples")
+    assert_bitwise(g["u"], oracle.silu_bf16(h["temb"]), "1x4096 chunk: u")
+    check_rows(h["x"], h["dy"], g["emb"], g, oracle, what="1x4096 chunk: sampled samples")
+    prod = oracle.bwd_products_f32(h["dy"], h["x"], g["mean"], g["rstd"])
+    assert_bitwise(g["d_emb"], oracle.token_tree_f32(prod), "1x4096 chunk: d_emb vs the fp32 tree")
+    _, w_demb = oracle.out_bwd(h["dy"], h["x"], g["emb"])
+    check_f32(g["d_emb"], w_demb, floor_d_emb(bf16_to_f64(h["x"]), bf16_to_f64(h["dy"])), what="1x4096 chunk: d_emb")
+    w_dt, _, _ = oracle.proj_bwd(g["d_emb"], h["temb"], W, want_dW=False)
+    from invariant_dit_adaln_gb300 import synth
+    fl = floor_d_temb(bf16_to_f64(synth.bf16_bits_from_f32(g["d_emb"])), bf16_to_f64(W),
+                      oracle.dsilu_f64(bf16_to_f64(h["temb"])))
+    check_bf16(g["d_temb"], w_dt, fl, what="1x4096 chunk: d_temb")
+    sW, sb = oracle.wgrad_seq_f32_rows(host_f32(ref["d_emb"]), host_bf16(dev["temb"]), np.array(rows, np.int32))
+    assert_bitwise(host_f32(refW)[rows], sW, "1x4096 chunk: sampled rows of dW")
+    assert_bitwise(host_f32(refb)[rows], sb, "1x4096 chunk: sampled rows of db")
+
+
 @pytest.mark.slow
 def test_chunking_invariance_full_workload():
-    """4096 samples of S=256 as 1x4096, 2x2048, 16x256, 64x64 and 4096x1."""
+    """4096 samples of S=256 as 1x4096, 2x2048, 16x256, 64x64 and 4096x1; the
+    1x4096 chunk also against the oracle on 8 samples and 16 rows of dW."""
     D, S, n = 3072, 256, 4096
     dev = _device_inputs(n, S, D, seed=6)
     ref, refW, refb = _chunked(dev, 4096, D)
+    _oracle_check_samples(dev, ref, refW, refb, samples=[0, 1, 977, 2048, 2049, 3333, 4094, 4095],
+                          rows=[0, 1, 255, 256, 1000, 3071, 3072, 3073, 4095, 4096, 5000, 6000, 6142, 6143, 77, 2222],
+                          D=D)
     for c in [2048, 256, 64, 1]:
         got, gW, gb = _chunked(dev, c, D)
         for k in PER_SAMPLE:

@@ -5,8 +5,8 @@ Both lengths end in a ragged tile (16 and 9 tokens) and fold through three
 tree levels.  d_emb is compared bit for bit against the fp32 replay of the
 token tree and within tolerance against the fp64 sums; dW and db bit for bit
 against the sequential fp32 replay over the samples; d_temb and emb in full;
-out, mean, rstd and dx on sampled rows (tile edges, the ragged last tile,
-outlier rows and seeded random rows), each computed by the oracle row by row."""
+out, mean, rstd and dx over every token row (the oracle fed the GPU's emb),
+with at most 1e-5 of the elements passing only through their floor."""
 
 from __future__ import annotations
 
@@ -17,8 +17,7 @@ import torch
 import oracle
 from invariant_dit_adaln_gb300 import binding, synth
 from gpu_util import host_bf16, host_f32, lib, run_step, to_device
-from tolerance import (F_RED, assert_bitwise, bf16_to_f64, check_bf16, check_f32, floor_d_emb, floor_d_temb, floor_dx,
-                       floor_out)
+from tolerance import assert_bitwise, bf16_to_f64, check_bf16, check_f32, check_rows, floor_d_emb, floor_d_temb
 
 pytestmark = pytest.mark.gpu
 
@@ -37,39 +36,15 @@ def run(request):
     return S, inp, {k: (host_bf16(v) if v.dtype == torch.bfloat16 else host_f32(v)) for k, v in r.items()}
 
 
-def _sample_rows(S, inp):
-    rng = np.random.default_rng(S)
-    last = (S - 1) // 32 * 32  # first token of the ragged last tile
-    rows = {0, 31, 32, 1023, 1024, last - 1, last, S - 2, S - 1}
-    picked = {(int(f) // S, int(f) % S) for f in inp["outlier_rows"][:6]}
-    for b in range(B):
-        picked |= {(b, s) for s in rows}
-        picked |= {(b, int(s)) for s in rng.integers(0, S, 6)}
-    return sorted(picked)
-
-
 def test_emb_and_u(run):
     S, inp, g = run
     check_bf16(g["emb"], oracle.proj_fwd(inp["temb"], inp["W"], inp["b"]), what="emb")
     assert_bitwise(g["u"], oracle.silu_bf16(inp["temb"]), "u")
 
 
-def test_out_and_dx_sampled_rows(run):
+def test_out_and_dx_all_rows(run):
     S, inp, g = run
-    emb = g["emb"]
-    onep_all = bf16_to_f64(synth.bf16_bits_from_f32(np.float32(1) + bf16_to_f64(emb[:, :D]).astype(np.float32)))
-    for b, s in _sample_rows(S, inp):
-        x = inp["x"][b:b + 1, s:s + 1]
-        dy = inp["dy"][b:b + 1, s:s + 1]
-        e = emb[b:b + 1]
-        onep, shift = onep_all[b:b + 1], bf16_to_f64(e[:, D:])
-        xf = bf16_to_f64(x)
-        w_out, w_mean, w_rstd = oracle.out_fwd(x, e)
-        check_bf16(g["out"][b:b + 1, s:s + 1], w_out, floor_out(xf, onep, shift), what=f"out row ({b},{s})")
-        check_f32(g["mean"][b:b + 1, s:s + 1], w_mean, F_RED * np.abs(xf).mean(-1), what="mean")
-        check_f32(g["rstd"][b:b + 1, s:s + 1], w_rstd, what="rstd")
-        w_dx, _ = oracle.out_bwd(dy, x, e)
-        check_bf16(g["dx"][b:b + 1, s:s + 1], w_dx, floor_dx(xf, bf16_to_f64(dy), onep), what=f"dx row ({b},{s})")
+    check_rows(inp["x"], inp["dy"], g["emb"], g, oracle, what=f"B={B} S={S}")
 
 
 def test_d_emb(run):

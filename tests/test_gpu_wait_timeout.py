@@ -1,0 +1,74 @@
+"""The time-out path of the kernels' waits, run on the GPU without a fault.
+
+Kernels that wait on their own bulk copies give each wait a time limit; a wait
+that runs out sets the library's device error word and the kernel drains the
+copies it issued, then returns.  A test build of the library sends the first
+wait of every waiting kernel to an mbarrier that nothing ever arrives on (a
+200 us limit), so the path runs: the forward reports 0x101, the backward 0x201,
+no drain runs out (the 0x8000 bit stays clear), and the GPU context stays
+usable, shown by the release library's results afterwards being the same bytes
+as before.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+import torch
+
+from invariant_dit_adaln_gb300 import binding, build, synth
+from gpu_util import run_step, to_device
+
+pytestmark = pytest.mark.gpu
+
+FWD_WAIT, BWD_WAIT, DRAIN_FAILED = 0x101, 0x201, 0x8000
+
+
+@pytest.fixture(scope="module")
+def wait_lib():
+    path = build.build(extra_flags=build.WAIT_TEST_FLAGS, variant="waittest")
+    L = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.adaln_out_fwd.argtypes = [P, P, P, P, P, I, I, I, ctypes.c_float, P]
+    L.adaln_out_bwd.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_size_t, I, I, I, P]
+    L.adaln_device_error.restype = I
+    return L
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+@pytest.mark.parametrize("B,S,D", [(2, 100, 3072), (1, 40, 8192)])
+def test_waits_that_run_out_report_and_return(wait_lib, B, S, D):
+    L = wait_lib
+    binding.load()
+    inp = to_device(synth.make_inputs(B, S, D, 3, outlier_frac=0.01))
+    before = run_step(inp)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    emb = before["emb"]
+    out = torch.empty_like(inp["x"])
+    mean = torch.empty((B, S), dtype=torch.float32, device="cuda")
+    rstd = torch.empty_like(mean)
+    st = torch.cuda.current_stream().cuda_stream
+    assert L.adaln_out_fwd(inp["x"].data_ptr(), emb.data_ptr(), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                           B, S, D, 1e-6, st) == 0
+    err = L.adaln_device_error()
+    assert err & ~DRAIN_FAILED == FWD_WAIT and not err & DRAIN_FAILED, hex(err)
+    dx = torch.empty_like(inp["x"])
+    d_emb = torch.empty((B, 2 * D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.adaln_out_bwd_workspace_bytes(B, S, D), dtype=torch.uint8, device="cuda")
+    assert L.adaln_out_bwd(inp["dy"].data_ptr(), inp["x"].data_ptr(), emb.data_ptr(), before["mean"].data_ptr(),
+                           before["rstd"].data_ptr(), dx.data_ptr(), d_emb.data_ptr(), ws.data_ptr(), ws.numel(),
+                           B, S, D, st) == 0
+    err = L.adaln_device_error()
+    assert err & ~DRAIN_FAILED == BWD_WAIT and not err & DRAIN_FAILED, hex(err)
+    assert L.adaln_device_error() == 0  # read and cleared
+    # the context is still usable: the release library gives the same bytes
+    after = run_step(inp)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    for k, v in before.items():
+        assert torch.equal(_bits(after[k]), _bits(v)), k

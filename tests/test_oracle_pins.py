@@ -456,6 +456,71 @@ def test_token_sum_f64_is_correctly_rounded(orc):
             assert got[b, h] == math.fsum(a[b, :, h].astype(np.float64))
 
 
+def f32_exact_round(v: Fraction) -> Fraction:
+    """The fp32 value nearest to the rational v (ties to even), as a rational."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    # a in [2^e, 2^(e+1)); spacing 2^(e-23) for normals, 2^-149 below 2^-126
+    q = max(e - 23, -149)
+    scaled = a / (Fraction(2) ** q)
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    r = Fraction(n) * Fraction(2) ** q
+    return r if v > 0 else -r
+
+
+def test_f32_exact_round_agrees_with_ieee_single():
+    """The helper above against numpy's own fp32 conversion of fp64 values
+    (one rounding), including ties, near-ties and subnormals."""
+    rng = np.random.default_rng(30)
+    vals = list(rng.standard_normal(2000) * np.exp2(rng.integers(-160, 120, 2000)))
+    for k in range(1, 200, 3):
+        tie = 1.0 + (2 * k + 1) * 2.0 ** -24
+        vals += [tie, -tie, np.nextafter(tie, 10), np.nextafter(tie, 0)]
+    vals += [2.0 ** -149, 2.0 ** -150, 3 * 2.0 ** -151, 1.5 * 2.0 ** -126]
+    for v in vals:
+        assert float(f32_exact_round(Fraction(float(v)))) == float(np.float32(v)), v
+
+
+def test_bwd_products_two_roundings_at_nonzero_mean(orc):
+    """The scale-tree product p = fp32(g * fp32(fp32(x - mean) * rstd)) from the
+    forward's saved statistics, pinned bit for bit against exact rationals with
+    an RNE rounding after the subtraction, after the multiply by rstd and after
+    the multiply by g.  The inputs (mean with a full fp32 significand, rstd far
+    from 1, and x near the mean where x - mean loses bits) are chosen so that
+    the plausible wrong orders give different bits: x rstd - mean rstd, x - mean
+    kept exact, and a single rounding of the exact product."""
+    rng = np.random.default_rng(31)
+    B, S, D = 1, 64, 64
+    mean = (rng.standard_normal((B, S)) * 3 + rng.uniform(-1, 1, (B, S)) * 1e-3).astype(np.float32)
+    rstd = np.exp(rng.uniform(-4, 4, (B, S))).astype(np.float32)
+    near = mean[..., None] + rng.standard_normal((B, S, D)) * np.exp2(rng.integers(-12, 2, (B, S, D)))
+    x = synth.bf16_bits_from_f32(near.astype(np.float32))
+    dy = synth.bf16_bits_from_f32((rng.standard_normal((B, S, D)) * 2).astype(np.float32))
+    got = orc.bwd_products_f32(dy, x, mean, rstd)
+    xf, gf = bf16_to_f64(x), bf16_to_f64(dy)
+    R = f32_exact_round
+    differ = {"x*rstd - mean*rstd": 0, "x - mean exact": 0, "one rounding": 0}
+    for s in range(S):
+        m, r = Fraction(float(mean[0, s])), Fraction(float(rstd[0, s]))
+        for d in range(D):
+            xv, gv = Fraction(float(xf[0, s, d])), Fraction(float(gf[0, s, d]))
+            want = R(gv * R(R(xv - m) * r))
+            assert Fraction(float(got[0, s, d])) == want, (s, d)
+            assert Fraction(float(got[0, s, D + d])) == gv
+            differ["x*rstd - mean*rstd"] += R(gv * R(R(xv * r) - R(m * r))) != want
+            differ["x - mean exact"] += R(gv * R((xv - m) * r)) != want
+            differ["one rounding"] += R(gv * (xv - m) * r) != want
+    # every wrong order is caught by this input set
+    assert all(v > 0 for v in differ.values()), differ
+
+
 def test_bwd_products_reuse_forward_statistics(orc):
     """prod = (g * fp32(fp32(x - mean) * rstd), g): with mean 0 and rstd 1 the
     product is g * x exactly; the shift half is g."""
@@ -537,3 +602,23 @@ def test_wgrad_seq_f32_order_and_chunking(orc):
     _, dW64, db64 = orc.proj_bwd(d_emb, temb, W)
     bound = (B - 1) * 2.0 ** -24 * (np.abs(e).T @ np.abs(u))
     assert np.all(np.abs(full - dW64) <= bound + 1e-30)
+
+
+def test_wgrad_seq_f32_rows(orc):
+    """The sampled-rows form: B = 1 gives the exact outer product of the
+    listed rows; with many samples, the listed rows of the full sequential
+    accumulation, bit for bit."""
+    rng = np.random.default_rng(22)
+    B, D = 9, 24
+    temb = _bf16(rng.standard_normal((B, D)))
+    d_emb = rng.standard_normal((B, 2 * D)).astype(np.float32)
+    rows = np.array([0, 5, 2 * D - 1, 17, 5], np.int32)
+    e = bf16_to_f64(synth.bf16_bits_from_f32(d_emb))
+    u = bf16_to_f64(orc.silu_bf16(temb))
+    dW1, db1 = orc.wgrad_seq_f32_rows(d_emb[:1], temb[:1], rows)
+    assert_bitwise(dW1, np.outer(e[0, rows], u[0]).astype(np.float32), "B=1 rows")
+    assert_bitwise(db1, e[0, rows].astype(np.float32), "B=1 db rows")
+    full, fullb = orc.wgrad_seq_f32(d_emb, temb)
+    got, gotb = orc.wgrad_seq_f32_rows(d_emb, temb, rows)
+    assert_bitwise(got, full[rows], "rows of the full accumulation")
+    assert_bitwise(gotb, fullb[rows], "rows of db")
