@@ -119,7 +119,6 @@ adaln_status check_out_bwd_args(const void *dy, const void *x, const void *emb, 
 }
 
 cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &dev) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
     static std::unordered_map<const void *, size_t> done[64];
     const int slot = dev.device & 63;
     {
@@ -127,6 +126,7 @@ cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &d
         auto it = done[slot].find(func);
         if (it != done[slot].end() && it->second >= bytes) return cudaSuccess;
     }
+    if (bytes <= 48 * 1024) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -279,7 +279,11 @@ adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const ad
 
 int adaln_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    return read_and_clear_device_error();
+    // the LayerNorm kernels' word first, then the projection kernels'; both cleared
+    const int a = read_and_clear_device_error();
+    const int b = read_and_clear_proj_error();
+    if (a < 0 || b < 0) return -1;
+    return a != 0 ? a : b;
 }
 
 }  // extern "C"

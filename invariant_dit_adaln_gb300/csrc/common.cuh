@@ -27,6 +27,7 @@ enum DeviceError : unsigned {
     kErrNone = 0,
     kErrOutFwdWait = 0x101,
     kErrOutBwdWait = 0x201,
+    kErrProjFwdWait = 0x301,
     kErrDrainFailed = 0x8000,  // or-ed in: an issued copy did not land while leaving
 };
 
@@ -350,6 +351,19 @@ __device__ __forceinline__ void stg16_hint(void *p, uint4 v, uint64_t pol) {
                  "r"(v.z), "r"(v.w), "l"(pol)
                  : "memory");
 }
+// 16-byte fp32 store with an L2 policy
+__device__ __forceinline__ void stg16f_hint(void *p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
+// fp32 load with an L2 policy (coherent at L2: reads what an earlier kernel wrote)
+__device__ __forceinline__ float ldcg_hint(const float *p, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
 // bulk copy global -> shared with an L2 policy (as bulk_g2s)
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                               uint64_t pol) {

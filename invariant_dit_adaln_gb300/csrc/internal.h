@@ -30,7 +30,11 @@ cudaError_t ensure_smem_attr(const void *func, size_t bytes, const DeviceInfo &d
 
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while the preceding kernel on the stream finishes; every kernel of this
-// library calls griddepcontrol.wait before touching global memory.
+// library calls griddepcontrol.wait before reading what a preceding kernel may
+// write.  Every launch also asks for the largest shared-memory carve-out, so
+// that consecutive kernels of the library never wait for an SM to change its
+// L1/shared-memory split (which would also keep a dependent grid from starting
+// early).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args... args) {
@@ -39,11 +43,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+    attr[1].val.sharedMemCarveout = (unsigned)cudaSharedmemCarveoutMaxShared;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
@@ -63,5 +69,6 @@ cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint1
 cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
                             uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
                             int accumulate, void *ws, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
+int read_and_clear_proj_error();
 
 }  // namespace adaln

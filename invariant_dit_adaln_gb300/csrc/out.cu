@@ -839,25 +839,28 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         }
         return;
     }
-    // level-0 node of this tile: scale half at columns [0, D), shift half at [D, 2D)
+    // level-0 node of this tile: scale half at columns [0, D), shift half at [D, 2D);
+    // kept in L2 (evict-last) for the fold that reads it next
     const int H = 2 * D;
     float *ps = ws_sig + ((size_t)b * T + tile) * H;
     float *pk = ws_kap + ((size_t)b * T + tile) * H;
+    const uint64_t pol_keep = l2_evict_last();
+    auto put = [&](float *dst, px2 a, px2 c) {
+        stg16f_hint(dst, make_float4(px_lo(a), px_hi(a), px_lo(c), px_hi(c)), pol_keep);
+    };
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
         if (EXACT || v < V) {
             const size_t c = (size_t)v * 8;
-            stg16f(ps + c, make_float4(px_lo(sg_s[j][0]), px_hi(sg_s[j][0]), px_lo(sg_s[j][1]), px_hi(sg_s[j][1])));
-            stg16f(ps + c + 4, make_float4(px_lo(sg_s[j][2]), px_hi(sg_s[j][2]), px_lo(sg_s[j][3]), px_hi(sg_s[j][3])));
-            stg16f(pk + c, make_float4(px_lo(kp_s[j][0]), px_hi(kp_s[j][0]), px_lo(kp_s[j][1]), px_hi(kp_s[j][1])));
-            stg16f(pk + c + 4, make_float4(px_lo(kp_s[j][2]), px_hi(kp_s[j][2]), px_lo(kp_s[j][3]), px_hi(kp_s[j][3])));
-            stg16f(ps + D + c, make_float4(px_lo(sg_h[j][0]), px_hi(sg_h[j][0]), px_lo(sg_h[j][1]), px_hi(sg_h[j][1])));
-            stg16f(ps + D + c + 4,
-                   make_float4(px_lo(sg_h[j][2]), px_hi(sg_h[j][2]), px_lo(sg_h[j][3]), px_hi(sg_h[j][3])));
-            stg16f(pk + D + c, make_float4(px_lo(kp_h[j][0]), px_hi(kp_h[j][0]), px_lo(kp_h[j][1]), px_hi(kp_h[j][1])));
-            stg16f(pk + D + c + 4,
-                   make_float4(px_lo(kp_h[j][2]), px_hi(kp_h[j][2]), px_lo(kp_h[j][3]), px_hi(kp_h[j][3])));
+            put(ps + c, sg_s[j][0], sg_s[j][1]);
+            put(ps + c + 4, sg_s[j][2], sg_s[j][3]);
+            put(pk + c, kp_s[j][0], kp_s[j][1]);
+            put(pk + c + 4, kp_s[j][2], kp_s[j][3]);
+            put(ps + D + c, sg_h[j][0], sg_h[j][1]);
+            put(ps + D + c + 4, sg_h[j][2], sg_h[j][3]);
+            put(pk + D + c, kp_h[j][0], kp_h[j][1]);
+            put(pk + D + c + 4, kp_h[j][2], kp_h[j][3]);
         }
     }
 }
@@ -932,17 +935,18 @@ __device__ __forceinline__ void fold_values(const float (&vs)[kTile], const floa
 __device__ __forceinline__ void fold_group(const float *sig, const float *kap, size_t stride, int count,
                                            float &out_s, float &out_k) {
     float vs[kTile], vk[kTile];
+    const uint64_t pol = l2_evict_first();  // the level-0 nodes are read once
     if (count == kTile) {
         // a full group: all 64 loads issued before the first add
 #pragma unroll
-        for (int q = 0; q < kTile; ++q) vs[q] = __ldcg(sig + (size_t)q * stride);
+        for (int q = 0; q < kTile; ++q) vs[q] = ldcg_hint(sig + (size_t)q * stride, pol);
 #pragma unroll
-        for (int q = 0; q < kTile; ++q) vk[q] = __ldcg(kap + (size_t)q * stride);
+        for (int q = 0; q < kTile; ++q) vk[q] = ldcg_hint(kap + (size_t)q * stride, pol);
     } else {
 #pragma unroll
         for (int q = 0; q < kTile; ++q) {
-            vs[q] = q < count ? __ldcg(sig + (size_t)q * stride) : 0.0f;
-            vk[q] = q < count ? __ldcg(kap + (size_t)q * stride) : 0.0f;
+            vs[q] = q < count ? ldcg_hint(sig + (size_t)q * stride, pol) : 0.0f;
+            vk[q] = q < count ? ldcg_hint(kap + (size_t)q * stride, pol) : 0.0f;
         }
     }
     fold_values(vs, vk, count, out_s, out_k);

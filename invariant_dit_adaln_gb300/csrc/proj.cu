@@ -26,6 +26,15 @@ namespace adaln {
 // --------------------------------------------------------------------------
 static __device__ uint16_t g_silu_tab[65536];
 
+// device-side error word of this file's kernels (see adaln_device_error)
+static __device__ unsigned g_err_proj;
+__device__ __forceinline__ void report_error_proj(unsigned code) {
+    if (code == kErrDrainFailed)
+        atomicOr(&g_err_proj, code);
+    else
+        atomicCAS(&g_err_proj, 0u, code);
+}
+
 __global__ void __launch_bounds__(256) silu_table_kernel() {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < 65536) g_silu_tab[i] = silu_bf16((uint16_t)i);
@@ -251,6 +260,162 @@ proj_fwd_stream_kernel(const uint16_t *__restrict__ u, const uint16_t *__restric
 }
 
 // --------------------------------------------------------------------------
+// The projection for one or two samples (a diffusion step's batch) with all of
+// W requested at once: one CTA per SM, each owning a contiguous range of about
+// 2D / SMs rows.  Right after the dependency wait (and the small temb load),
+// each of the 16 warps loads one row into registers, and the warps issue bulk
+// copies of the CTA's other rows into shared memory (an mbarrier per copy), so
+// the whole of W is in flight in one wave; meanwhile every CTA computes u = bf16(silu(temb))
+// into shared memory (fp32, two float4 planes per sample).  Then each warp dots
+// its register row, and the shared-memory rows as they land.  The order of the
+// terms is the one above, so emb has the bits of the other kernels.
+// --------------------------------------------------------------------------
+constexpr int kWaveWarps = 16;
+constexpr int kWaveMaxSmemRows = 32;
+constexpr int kWaveChunkRows = 1;  // rows of W per bulk copy
+
+// u = bf16(silu(t)) with the table's bits: computed in fp32 where the fp32 value
+// is not near a bf16 rounding tie (the table holds that same value there), the
+// table itself elsewhere
+__device__ __forceinline__ uint32_t silu_fast(uint16_t tb) {
+    const float t = bf16f(tb);
+    if (t < -80.0f) return __ldg(&g_silu_tab[tb]);
+    const float s = __fdiv_rn(t, __fadd_rn(1.0f, expf(-t)));
+    const int low = (int)(__float_as_uint(s) & 0xFFFFu) - 0x8000;
+    if (low <= 16 && low >= -16) return __ldg(&g_silu_tab[tb]);
+    return bf16_bits(s);
+}
+
+template <int BC>
+__global__ void __launch_bounds__(kWaveWarps * 32, 1)
+proj_fwd_wave_kernel(const uint16_t *__restrict__ temb, const uint16_t *__restrict__ W,
+                     const uint16_t *__restrict__ bias, uint16_t *__restrict__ emb, uint16_t *__restrict__ u_out,
+                     int B, int D) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);          // [chunks of rows]
+    __shared__ int drain_needed;
+    float *uf = reinterpret_cast<float *>(smem_raw + 256);            // [BC][D]
+    unsigned char *wrows = smem_raw + 256 + (size_t)BC * D * 4;      // [rows][D] bf16
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = 2 * D;
+    const int V = D >> 3;
+    const int row_bytes = D * 2;
+    const int r_begin = (int)(((long long)blockIdx.x * N) / gridDim.x);
+    const int r_end = (int)(((long long)(blockIdx.x + 1) * N) / gridDim.x);
+    const int nrows = r_end - r_begin;
+    const int nreg = min(nrows, kWaveWarps);  // rows held in registers, one per warp
+    const int nsm = nrows - nreg;             // rows staged in shared memory (the host checks the bound)
+
+    if (threadIdx.x == 0) {
+        for (int c = 0; c * kWaveChunkRows < nsm; ++c) mbar_init(&full[c], 1);
+        drain_needed = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();  // temb, W and bias may come from the preceding kernel
+    pdl_trigger();
+    // temb first (12 KB per sample), so that it does not queue behind W
+    constexpr int kTembPerThread = 2;  // B * D / 8 <= 768 vectors over 512 threads (the host checks)
+    uint4 tv[kTembPerThread];
+#pragma unroll
+    for (int q = 0; q < kTembPerThread; ++q) {
+        const int i = threadIdx.x + q * (int)blockDim.x;
+        tv[q] = i < B * V ? ldg16(temb + (size_t)i * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint64_t pol_w = l2_evict_last();  // the backward projection reads W again
+    // this warp's register row first (loads issued behind a burst of bulk
+    // copies wait for it), then the shared-memory rows: consecutive rows of W,
+    // so they go in copies of kWaveChunkRows rows, issued by different warps
+    uint4 wr[kStreamVL];
+    const bool has_reg = warp < nreg;
+    const int nr = r_begin + warp;
+#pragma unroll
+    for (int j = 0; j < kStreamVL; ++j) {
+        const int v = lane + 32 * j;
+        wr[j] = (has_reg && v < V) ? ldg16_hint(W + (size_t)nr * D + (size_t)v * 8, pol_w) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int nchunk = (nsm + kWaveChunkRows - 1) / kWaveChunkRows;
+    if (lane == 0)
+        for (int c = warp; c < nchunk; c += kWaveWarps) {
+            const int i0 = c * kWaveChunkRows;
+            const uint32_t bytes = (uint32_t)min(kWaveChunkRows, nsm - i0) * row_bytes;
+            mbar_arrive_expect_tx(&full[c], bytes);
+            bulk_g2s_hint(wrows + (size_t)i0 * row_bytes, W + (size_t)(r_begin + nreg + i0) * D, bytes, &full[c], pol_w);
+        }
+    // u of every sample as fp32 planes (columns 0-3, then 4-7 of every vector);
+    // the first CTA also writes u out
+#pragma unroll
+    for (int q = 0; q < kTembPerThread; ++q) {
+        const int i = threadIdx.x + q * (int)blockDim.x;
+        if (i >= B * V) break;
+        const uint4 t = tv[q];
+        const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
+        uint32_t uw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) uw[q] = silu_fast((uint16_t)(tw[q] & 0xFFFFu)) | (silu_fast((uint16_t)(tw[q] >> 16)) << 16);
+        const int bi = i / V, vi = i - bi * V;
+        float4 *dst = reinterpret_cast<float4 *>(uf + (size_t)bi * D);
+        dst[vi] = make_float4(bf16lo(uw[0]), bf16hi(uw[0]), bf16lo(uw[1]), bf16hi(uw[1]));
+        dst[V + vi] = make_float4(bf16lo(uw[2]), bf16hi(uw[2]), bf16lo(uw[3]), bf16hi(uw[3]));
+        if (blockIdx.x == 0) stg16(u_out + (size_t)i * 8, make_uint4(uw[0], uw[1], uw[2], uw[3]));
+    }
+    __syncthreads();
+
+    auto row_out = [&](const uint4(&w)[kStreamVL], int n) {
+        float2 acc[BC];
+#pragma unroll
+        for (int b = 0; b < BC; ++b) acc[b] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < kStreamVL; ++j) {
+            const int v = lane + 32 * j;
+            if (v < V) {
+#pragma unroll
+                for (int b = 0; b < BC; ++b) {
+                    if (b < B) {
+                        const float4 *up = reinterpret_cast<const float4 *>(uf + (size_t)b * D);
+                        const float4 ua = up[v], ub = up[V + v];
+                        acc[b] = dot_pairs(w[j], make_float2(ua.x, ua.y), make_float2(ua.z, ua.w),
+                                           make_float2(ub.x, ub.y), make_float2(ub.z, ub.w), acc[b]);
+                    }
+                }
+            }
+        }
+        const float bn = bf16f(bias[n]);
+#pragma unroll
+        for (int b = 0; b < BC; ++b) {
+            if (b < B) {
+                const float tot = warp_sum(__fadd_rn(acc[b].x, acc[b].y));
+                if (lane == 0) emb[(size_t)b * N + n] = bf16_bits(__fadd_rn(tot, bn));
+            }
+        }
+    };
+    if (has_reg) row_out(wr, nr);
+    for (int i = warp; i < nsm; i += kWaveWarps) {
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[i / kWaveChunkRows], 0u));
+        if (!ok) {
+            if (lane == 0) {
+                report_error_proj(kErrProjFwdWait);
+                drain_needed = 1;
+            }
+            break;
+        }
+        uint4 ws[kStreamVL];
+        const uint4 *src = reinterpret_cast<const uint4 *>(wrows + (size_t)i * row_bytes);
+#pragma unroll
+        for (int j = 0; j < kStreamVL; ++j) {
+            const int v = lane + 32 * j;
+            ws[j] = v < V ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        row_out(ws, r_begin + nreg + i);
+    }
+    __syncthreads();
+    if (drain_needed && threadIdx.x == 0)  // let every issued copy land before leaving
+        for (int c = 0; c * kWaveChunkRows < nsm; ++c)
+            if (!mbar_wait_bounded(&full[c], 0u, 10000000ull)) report_error_proj(kErrDrainFailed);
+}
+
+// --------------------------------------------------------------------------
 // Backward, kernel 1: one CTA per (k-chunk of 256 columns, slab of 256 rows).
 //
 // Warp w takes the slab's rows n = n0 + w + 8 i (i ascending), lane l the 8
@@ -428,7 +593,7 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                 float tot = sm.red[0][b][c];
 #pragma unroll
                 for (int w = 1; w < 8; ++w) tot = __fadd_rn(tot, sm.red[w][b][c]);
-                ws[((size_t)slab * B + b0 + b) * D + k] = tot;
+                __stcg(ws + ((size_t)slab * B + b0 + b) * D + k, tot);
             }
         }
         __syncthreads();
@@ -448,15 +613,27 @@ proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
     if (i < BD) {
-        // all partials are loaded before the first add (nslab <= kMaxSlabs)
-        float part[kMaxSlabs];
+        const float ds = dsilu_f32(bf16f(temb[i]));
+        float tot;
+        if (nslab == 24) {
+            // D = 3072: all 24 partials requested before the first add
+            float part[24];
 #pragma unroll
-        for (int s = 0; s < kMaxSlabs; ++s) part[s] = s < nslab ? ws[(size_t)s * BD + i] : 0.0f;
-        float tot = part[0];
+            for (int s = 0; s < 24; ++s) part[s] = __ldcg(ws + (size_t)s * BD + i);
+            tot = part[0];
 #pragma unroll
-        for (int s = 1; s < kMaxSlabs; ++s)
-            if (s < nslab) tot = __fadd_rn(tot, part[s]);
-        d_temb[i] = bf16_bits(__fmul_rn(tot, dsilu_f32(bf16f(temb[i]))));
+            for (int s = 1; s < 24; ++s) tot = __fadd_rn(tot, part[s]);
+        } else {
+            // all partials are loaded before the first add (nslab <= kMaxSlabs)
+            float part[kMaxSlabs];
+#pragma unroll
+            for (int s = 0; s < kMaxSlabs; ++s) part[s] = s < nslab ? __ldcg(ws + (size_t)s * BD + i) : 0.0f;
+            tot = part[0];
+#pragma unroll
+            for (int s = 1; s < kMaxSlabs; ++s)
+                if (s < nslab) tot = __fadd_rn(tot, part[s]);
+        }
+        d_temb[i] = bf16_bits(__fmul_rn(tot, ds));
     }
 }
 
@@ -589,13 +766,34 @@ static cudaError_t ensure_silu_table(cudaStream_t stream, const DeviceInfo &dev)
     return err;
 }
 
-// The SiLU kernel, then: up to kStreamMaxB samples and D <= 3072, the
-// streaming GEMV; otherwise the chunked GEMV.
+template <int BC>
+static cudaError_t launch_proj_fwd_wave(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
+                                        uint16_t *u, int B, int D, size_t smem, cudaStream_t stream,
+                                        const DeviceInfo &dev) {
+    auto kern = proj_fwd_wave_kernel<BC>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(dev.sm_count), dim3(kWaveWarps * 32), smem, stream, temb, W, bias, emb, u, B, D);
+}
+
+// One or two samples with D <= 3072 (when every SM can hold its share of W):
+// the one-wave kernel.  Otherwise the SiLU kernel, then: up to kStreamMaxB
+// samples and D <= 3072, the streaming GEMV; otherwise the chunked GEMV.
 cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
                             uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
     if (B == 0) return cudaSuccess;
     cudaError_t err = ensure_silu_table(stream, dev);
     if (err != cudaSuccess) return err;
+    if (B <= 2 && D / 8 <= 32 * kStreamVL && dev.sm_count > 0 && B * (D / 8) <= 2 * kWaveWarps * 32) {
+        const int N = 2 * D;
+        const int rows_max = (N + dev.sm_count - 1) / dev.sm_count;
+        const int nsm_max = rows_max > kWaveWarps ? rows_max - kWaveWarps : 0;
+        const size_t smem = 256 + (size_t)(B == 1 ? 1 : 2) * D * 4 + (size_t)nsm_max * D * 2;
+        if (nsm_max <= kWaveMaxSmemRows && smem <= 227 * 1024) {
+            if (B == 1) return launch_proj_fwd_wave<1>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+            return launch_proj_fwd_wave<2>(temb, W, bias, emb, u, B, D, smem, stream, dev);
+        }
+    }
     const long long n8 = (long long)B * D / 8;
     err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
     if (err != cudaSuccess) return err;
@@ -660,6 +858,13 @@ cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint
     const long long BD = (long long)B * D;
     return launch_pdl(proj_bwd_final_kernel, dim3((unsigned)((BD + 255) / 256)), dim3(256), 0, stream, ws, temb,
                       d_temb, B, D, nslab);
+}
+
+int read_and_clear_proj_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_proj, sizeof(v)) != cudaSuccess) return -1;
+    if (v != 0 && cudaMemcpyToSymbol(g_err_proj, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    return (int)v;
 }
 
 }  // namespace adaln
