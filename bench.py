@@ -10,6 +10,7 @@ oracle's throughput and the SM clocks seen during the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
     python bench.py --proj-sweep      # the projection calls alone, B = 1 .. 2048
+    python bench.py --chunking        # 4096 samples of S=256 in five chunkings
 
 Under torchrun (N > 1) every rank runs its own replica (weak scaling; the
 path has no cross-sample exchange), the elapsed time is the max over ranks
@@ -37,11 +38,13 @@ METRIC = "AdaLN-out fwd+bwd tokens/s and HBM GB/s (% of 8 TB/s) at B=2,S=4096,D=
 WORKLOAD = dict(B=2, S=4096, D=3072, seed=0, outlier_frac=0.01)
 NOMINAL_HBM_GBS = 8000.0
 FLUSH_BYTES = 512 << 20
-KERNELS_PER_STEP = 7  # SiLU, projection, out_fwd, bwd tile, tree fold, proj-bwd slab, d_temb
-# DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold) at this
-# workload, from the ncu capture summarised in profiles/out_bwd_B2_S4096_D3072.md.  The
-# counters of a replayed launch miss the dx lines still in L2 when it ends.
-OUT_BWD_DRAM_BYTES = 133_192_704
+# kernels per step at this workload: projection, LayerNorm forward, backward
+# tile, tree fold, projection-backward slab, d_temb
+KERNELS_PER_STEP = 6
+# DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold)
+# at this workload, from one ncu capture of the current kernels (dram__bytes_read.sum
+# + dram__bytes_write.sum); None when the kernels changed after the capture.
+OUT_BWD_DRAM_BYTES = None
 
 
 # ---------------------------------------------------------------------------
@@ -110,7 +113,72 @@ def throughput(units_per_rank: float, world: int, seconds: float) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
+class NvmlSampler:
+    """SM clock, max clock, power and clock-event reasons of one GPU, read
+    through NVML every `period_s` seconds in a thread (reads only; no setting is
+    changed).  Each sample carries its time, so samples can be binned by pass."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id=None, index=0, period_s=0.005):
+        import ctypes
+        self.period = period_s
+        self.samples = []  # (t, sm_mhz, max_mhz, power_w, reasons bitmask)
+        self._stop = threading.Event()
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.L = L
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = L.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle")
+        self.c = ctypes
+
+    def _read(self):
+        c, L = self.c, self.L
+        sm, mx, pw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        L.nvmlDeviceGetClockInfo(self.h, 1, c.byref(sm))        # NVML_CLOCK_SM
+        L.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
+        L.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        (getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or
+         L.nvmlDeviceGetCurrentClocksThrottleReasons)(self.h, c.byref(rs))
+        return (time.perf_counter(), float(sm.value), float(mx.value), pw.value / 1000.0, int(rs.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        self.thread.join(timeout=5)
+
+    def summary(self, windows=None):
+        """Median SM clock etc. over the samples inside the (t0, t1) windows."""
+        sel = [x for x in self.samples if windows is None or any(a <= x[0] <= b for a, b in windows)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0, "source": "nvml"}
+        mask = 0
+        for x in sel:
+            mask |= x[4]
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+                "power_w_max": max(x[3] for x in sel),
+                "reasons": sorted(n for bit, n in self.REASONS.items() if mask & bit), "samples": len(sel),
+                "source": "nvml"}
+
+
 class ClockSampler:
+    """Fallback when NVML cannot be loaded: nvidia-smi every 20 ms."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -124,7 +192,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -136,14 +204,36 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        return summarize_clocks(self.lines)
+
+    def summary(self, windows=None):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        r = summarize_clocks(self.lines)
+        r["source"] = "nvidia-smi"
+        return r
+
+
+def clock_sampler(device_index):
+    """NVML sampler for the CUDA device (matched by PCI bus id), else nvidia-smi."""
+    bus = None
+    try:
+        import torch
+        pr = torch.cuda.get_device_properties(device_index)
+        if hasattr(pr, "pci_bus_id"):
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+    except Exception:
+        bus = None
+    try:
+        return NvmlSampler(pci_bus_id=bus, index=device_index)
+    except OSError:
+        return ClockSampler(device_index)
 
 
 def summarize_clocks(lines):
@@ -196,19 +286,100 @@ def oracle_sample_step(oracle, inp, frac, emb_full=None):
     return time.perf_counter() - t0
 
 
-def time_oracle(inp, budget_s=12.0, max_steps=50):
-    """Run the full oracle chain repeatedly for about budget_s seconds."""
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_SHARED = {}
+
+
+def _pool_init(specs):
+    """Worker start-up: attach to the inputs in shared memory, load the oracle."""
+    from multiprocessing import shared_memory
     import oracle
     oracle.build()
-    B, S, _ = inp["x"].shape
+    for k, (name, shape, dtype) in specs.items():
+        shm = shared_memory.SharedMemory(name=name)
+        _SHARED[k] = (shm, np.ndarray(shape, dtype=dtype, buffer=shm.buf))
+
+
+def _pool_share(args):
+    """One worker's share of the oracle step: its tokens [s0, s1) of every
+    sample through the LayerNorm forward and backward, and its projection rows
+    [n0, n1) forward and backward.  Returns its seconds."""
+    i, P = args
+    import oracle
+    x, dy, temb, W, b, emb = (_SHARED[k][1] for k in ("x", "dy", "temb", "W", "b", "emb"))
+    B, S, D = x.shape
+    s0, s1 = S * i // P, S * (i + 1) // P
+    n0, n1 = 2 * D * i // P, 2 * D * (i + 1) // P
+    t0 = time.perf_counter()
+    oracle.proj_fwd_rows(temb, W, b, n0, n1, emb=emb.copy())
+    xs, dys = np.ascontiguousarray(x[:, s0:s1]), np.ascontiguousarray(dy[:, s0:s1])
+    oracle.out_fwd(xs, emb)
+    _, d_emb = oracle.out_bwd(dys, xs, emb)
+    oracle.proj_bwd_rows(d_emb, temb, W, n0, n1)
+    return time.perf_counter() - t0
+
+
+def time_oracle(inp, budget_s=12.0, max_steps=50):
+    """The oracle as it stands on the host: full steps on one thread for about
+    budget_s / 3 seconds, then whole steps split over every host core (spawned
+    worker processes, each running the oracle chain on its own share of the
+    tokens and projection rows) for about 2 budget_s / 3 seconds."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    import oracle
+    oracle.build()
+    B, S, D = inp["x"].shape
     times = []
     t_start = time.perf_counter()
-    while not times or (time.perf_counter() - t_start < budget_s and len(times) < max_steps):
+    while not times or (time.perf_counter() - t_start < budget_s / 3 and len(times) < max_steps):
         times.append(oracle_sample_step(oracle, inp, 1.0))
-    total = sum(times)
-    return {"value": B * S * len(times) / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} full steps of B={B}, S={S} (all tokens, all projection rows), single thread",
-            "seconds": total}
+    single = B * S * len(times) / sum(times)
+    emb = oracle.proj_fwd(inp["temb"], inp["W"], inp["b"])
+    arrays = {"x": inp["x"], "dy": inp["dy"], "temb": inp["temb"], "W": inp["W"], "b": inp["b"], "emb": emb}
+    P = os.cpu_count() or 1
+    shms, specs = [], {}
+    try:
+        for k, a in arrays.items():
+            a = np.ascontiguousarray(a)
+            shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf)[...] = a
+            shms.append(shm)
+            specs[k] = (shm.name, a.shape, a.dtype.str)
+        walls = []
+        with mp.get_context("spawn").Pool(P, initializer=_pool_init, initargs=(specs,)) as pool:
+            # every map has a time limit: a pool whose workers cannot start would
+            # otherwise wait forever
+            limit = 10 * budget_s + 60
+            pool.map_async(_pool_share, [(i, P) for i in range(P)]).get(timeout=limit)  # warm-up
+            t_start = time.perf_counter()
+            while not walls or (time.perf_counter() - t_start < 2 * budget_s / 3 and len(walls) < max_steps):
+                w0 = time.perf_counter()
+                pool.map_async(_pool_share, [(i, P) for i in range(P)]).get(timeout=limit)
+                walls.append(time.perf_counter() - w0)
+    except (mp.TimeoutError, OSError) as e:
+        return {"value": single, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"{len(times)} full steps of B={B}, S={S}, single thread (the multi-process run failed: {e!r})",
+                "single_thread_value": single, "cpu_model": cpu_model(), "nproc": P}
+    finally:
+        for shm in shms:
+            shm.close()
+            shm.unlink()
+    value = B * S * len(walls) / sum(walls)
+    return {"value": value, "unit": "tokens/s", "cores": P, "kind": "oracle",
+            "sample": (f"{len(walls)} full steps of B={B}, S={S}, each split over {P} worker processes "
+                       f"(tokens and projection rows in {P} shares); single thread: {len(times)} full steps"),
+            "single_thread_value": single, "cpu_model": cpu_model(), "nproc": P, "seconds": sum(walls)}
 
 
 # ---------------------------------------------------------------------------
@@ -237,87 +408,134 @@ def run_gpu(args, world, rank, local):
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
-    x, dy, temb, W, b = (dev(host[k]) for k in ("x", "dy", "temb", "W", "b"))
-    emb = torch.empty((B, N), dtype=torch.bfloat16, device=device)
-    u = torch.empty((B, D), dtype=torch.bfloat16, device=device)
-    out = torch.empty((B, S, D), dtype=torch.bfloat16, device=device)
-    mean = torch.empty((B, S), dtype=torch.float32, device=device)
-    rstd = torch.empty((B, S), dtype=torch.float32, device=device)
-    dx = torch.empty_like(out)
-    d_emb = torch.empty((B, N), dtype=torch.float32, device=device)
-    d_temb = torch.empty((B, D), dtype=torch.bfloat16, device=device)
-    dW = torch.empty((N, D), dtype=torch.bfloat16, device=device)
-    db = torch.empty((N,), dtype=torch.bfloat16, device=device)
-    ws_bwd = torch.empty(binding.adaln_out_bwd_workspace_bytes(B, S, D), dtype=torch.uint8, device=device)
-    ws_proj = torch.empty(binding.adaln_proj_bwd_workspace_bytes(B, D), dtype=torch.uint8, device=device)
+    def make_set():
+        """The step's inputs (the same seeded values), outputs and workspaces in
+        buffers of their own: 138 MB of inputs per set, more than L2 holds."""
+        d = {k: dev(host[k]) for k in ("x", "dy", "temb", "W", "b")}
+        d.update(emb=torch.empty((B, N), dtype=torch.bfloat16, device=device),
+                 u=torch.empty((B, D), dtype=torch.bfloat16, device=device),
+                 out=torch.empty((B, S, D), dtype=torch.bfloat16, device=device),
+                 mean=torch.empty((B, S), dtype=torch.float32, device=device),
+                 rstd=torch.empty((B, S), dtype=torch.float32, device=device),
+                 dx=torch.empty((B, S, D), dtype=torch.bfloat16, device=device),
+                 d_emb=torch.empty((B, N), dtype=torch.float32, device=device),
+                 d_temb=torch.empty((B, D), dtype=torch.bfloat16, device=device),
+                 dW=torch.empty((N, D), dtype=torch.bfloat16, device=device),
+                 db=torch.empty((N,), dtype=torch.bfloat16, device=device),
+                 ws_bwd=torch.empty(binding.adaln_out_bwd_workspace_bytes(B, S, D), dtype=torch.uint8, device=device),
+                 ws_proj=torch.empty(binding.adaln_proj_bwd_workspace_bytes(B, D), dtype=torch.uint8, device=device))
+        return d
+
+    sets = [make_set(), make_set()]
+    A = sets[0]
+    x, dy, temb, W, b = A["x"], A["dy"], A["temb"], A["W"], A["b"]
+    emb, u, out, mean, rstd, dx = A["emb"], A["u"], A["out"], A["mean"], A["rstd"], A["dx"]
+    d_emb, d_temb, dW, db, ws_bwd, ws_proj = A["d_emb"], A["d_temb"], A["dW"], A["db"], A["ws_bwd"], A["ws_proj"]
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=device)
 
     def flush():
-        # Between steps, outside the timed events: write a buffer 4x the L2
-        # (no line of the step's inputs or outputs stays cached), then read
-        # another one, so the dirty lines of the write are written back here
-        # rather than inside the next step.
+        # Between steps of the flushed pass, outside its timed events: write a
+        # buffer 4x the L2 (no line of the step's inputs or outputs stays
+        # cached), then read another one, so the dirty lines of the write are
+        # written back here rather than inside the next step.
         flush_w.zero_()
         flush_r.max()
     stream = torch.cuda.current_stream(device)
 
-    def step(st=stream):
-        binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=st)
-        binding.adaln_out_fwd(x, emb, out=out, mean=mean, rstd=rstd, stream=st)
-        binding.adaln_out_bwd(dy, x, emb, mean, rstd, dx=dx, d_emb=d_emb, workspace=ws_bwd, stream=st)
-        binding.adaln_proj_bwd(d_emb, temb, u, W, d_temb=d_temb, dW=dW, db=db, workspace=ws_proj, stream=st)
+    def step_on(d, st=stream):
+        binding.adaln_proj_fwd(d["temb"], d["W"], d["b"], emb=d["emb"], u=d["u"], stream=st)
+        binding.adaln_out_fwd(d["x"], d["emb"], out=d["out"], mean=d["mean"], rstd=d["rstd"], stream=st)
+        binding.adaln_out_bwd(d["dy"], d["x"], d["emb"], d["mean"], d["rstd"], dx=d["dx"], d_emb=d["d_emb"],
+                              workspace=d["ws_bwd"], stream=st)
+        binding.adaln_proj_bwd(d["d_emb"], d["temb"], d["u"], d["W"], d_temb=d["d_temb"], dW=d["dW"], db=d["db"],
+                               workspace=d["ws_proj"], stream=st)
 
-    for _ in range(args.warmup):
-        flush()
-        step()
+    def step(st=stream):
+        step_on(A, st)
+
+    for i in range(args.warmup):
+        step_on(sets[i % 2])
     torch.cuda.synchronize()
     assert binding.device_error() == 0
 
-    # The step's seven launches captured once in a CUDA graph (after the
+    # The step's launches captured once per input set in a CUDA graph (after the
     # warm-up, which also filled the SiLU table); the programmatic dependent
-    # launch edges between the kernels are kept.  The timed loop replays it.
-    graph = None
+    # launch edges between the kernels are kept.  The timed loops replay them.
+    graphs = None
     if not args.eager:
-        graph = torch.cuda.CUDAGraph()
+        graphs = []
         cap = torch.cuda.Stream(device)
         cap.wait_stream(stream)
-        with torch.cuda.graph(graph, stream=cap):
-            step(torch.cuda.current_stream(device))
+        for d in sets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                step_on(d, torch.cuda.current_stream(device))
+            graphs.append(g)
         torch.cuda.synchronize()
         assert binding.device_error() == 0
 
-    def run_step():
-        if graph is not None:
-            graph.replay()
+    def run_step(i):
+        if graphs is not None:
+            graphs[i % 2].replay()
         else:
-            step()
+            step_on(sets[i % 2])
 
-    # ---- timed region: K steps, per-step events, L2 flushed between steps ----
+    # ---- timed region: passes of exactly K steps back to back ----
+    # Consecutive steps alternate between the two input sets, each larger than
+    # L2, so no step finds its inputs cached by the step before.  One event pair
+    # on the launch stream brackets the K steps of a pass, with a barrier and a
+    # synchronize on both sides.  Passes repeat until about --min-timed-s
+    # seconds have been timed (the clocks are sampled throughout); the pass with
+    # the median time is reported, all passes are listed.
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    clocks = ClockSampler(local)
-    barrier(dist_mod, device)
-    torch.cuda.synchronize()
+    clocks = clock_sampler(local)
     clocks.start()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush()
-        starts[i].record(stream)
-        run_step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    barrier(dist_mod, device)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    my_time = sum(step_ms) / 1e3
+    passes, windows = [], []
+    t_begin = time.perf_counter()
+    while len(passes) < 3 or (time.perf_counter() - t_begin < args.min_timed_s and len(passes) < args.max_passes):
+        barrier(dist_mod, device)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(K):
+            run_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        windows.append((w0, time.perf_counter()))
+        barrier(dist_mod, device)
+        passes.append(e0.elapsed_time(e1) / 1e3)
+    wall = time.perf_counter() - t_begin
+    clocks.stop()
+    clk = clocks.summary(windows)
+    my_time = statistics.median(passes)
     t_max = max_over_ranks(my_time, dist_mod, device)
     assert binding.device_error() == 0
+    # the passes in ten consecutive bins: each bin's median time per step next to
+    # the median SM clock sampled over its span, and their product, so that any
+    # dependence on the clock shows
+    bins = []
+    nb = min(10, len(passes))
+    for k in range(nb):
+        lo, hi = k * len(passes) // nb, (k + 1) * len(passes) // nb
+        ms = statistics.median(passes[lo:hi]) / K * 1e3
+        mhz = clocks.summary([(windows[lo][0], windows[hi - 1][1])]).get("sm_mhz")
+        bins.append({"passes": hi - lo, "ms_per_step": ms, "sm_mhz": mhz,
+                     "ms_x_mhz": ms * mhz if mhz else None})
 
-    # the same steps launched one call at a time, for comparison
+    # ---- the same steps with the L2 flushed between them, one event pair per step ----
     K1 = min(K, 300)
+    fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K1)]
+    for i in range(K1):
+        flush()
+        fl[i][0].record(stream)
+        run_step(0)
+        fl[i][1].record(stream)
+    torch.cuda.synchronize()
+    flushed_ms = statistics.median(a.elapsed_time(c) for a, c in fl)
+
+    # ---- the same steps launched one call at a time ----
     eg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K1)]
     for i in range(K1):
         flush()
@@ -325,7 +543,7 @@ def run_gpu(args, world, rank, local):
         step()
         eg[i][1].record(stream)
     torch.cuda.synchronize()
-    eager_ms = statistics.mean(a.elapsed_time(c) for a, c in eg)
+    eager_ms = statistics.median(a.elapsed_time(c) for a, c in eg)
 
     # ---- per-call pass: events around each call (roofline of the dominant call) ----
     K2 = min(K, 300)
@@ -383,7 +601,7 @@ def run_gpu(args, world, rank, local):
         d["ws_proj"] = torch.empty_like(ws_proj)
         return d
 
-    sets = [dev_set(), dev_set()]
+    e2e_sets = [dev_set(), dev_set()]
 
     def ev(st):
         e = torch.cuda.Event()
@@ -399,7 +617,7 @@ def run_gpu(args, world, rank, local):
     stream.wait_event(t0)
     s_out.wait_event(t0)
     for i in range(K3):
-        d = sets[i % 2]
+        d = e2e_sets[i % 2]
         if free_in[i % 2] is not None:
             s_in.wait_event(free_in[i % 2])
         with torch.cuda.stream(s_in):
@@ -467,6 +685,8 @@ def run_gpu(args, world, rank, local):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": my_time / K * 1e3,
+        "ms_per_step_spread": {"min": min(passes) / K * 1e3, "max": max(passes) / K * 1e3, "passes": len(passes)},
+        "ms_per_step_flushed": flushed_ms,
         "ms_per_step_eager": eager_ms,
         "higher_is_better": True,
         "scaling": "weak",
@@ -476,10 +696,14 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic (seeded; x, dy ~ N(0,1) with 81 outlier rows x50; W, b ~ N(0, 0.02^2))",
         "config": {"workload": "AdaLN norm_out fwd+bwd, B=2 S=4096 D=3072, 1% outlier rows",
                    "B": B, "S": S, "D": D, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": ("eager: one C-ABI call at a time" if graph is None else
-                              "CUDA graph of the step's four C-ABI calls (7 kernels, programmatic launch edges), "
-                              "captured once after the warm-up and replayed each step"),
-                   "l2": "flushed between steps outside the timed events: 512 MiB write, then 512 MiB read (L2 cold and clean at each step start); inputs 138 MB > L2"},
+                   "launch": ("eager: one C-ABI call at a time" if graphs is None else
+                              "CUDA graphs of the step's four C-ABI calls (6 kernels, programmatic launch edges), "
+                              "one per input set, captured once after the warm-up; K steps replayed back to back"),
+                   "l2": ("inputs larger than L2: consecutive steps alternate between two copies of the inputs "
+                          "(138 MB each, L2 129 MB), no flush; ms_per_step_flushed: the same step with a 512 MiB "
+                          "write + 512 MiB read between steps, one event pair per step"),
+                   "timing": f"median of {len(passes)} passes of K={K} steps (one event pair per pass), "
+                             f"{wall:.2f} s timed in all"},
         "hbm_gbs": gbs,
         "hbm_frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
         "hbm_frac_of_measured": gbs / peak,
@@ -492,8 +716,8 @@ def run_gpu(args, world, rank, local):
         "step_roofline": {"achieved": gbs, "peak": peak, "frac": gbs / peak, "unit": "GB/s"},
         "e2e": {"value": throughput(tokens * K3, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * K,
-        "clocks": clk,
+        "gpu_launches": KERNELS_PER_STEP * K,  # in the reported pass of K steps
+        "clocks": {**clk, "bins": bins},
         "wall_s": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -614,6 +838,77 @@ def run_proj_sweep(args, rank, local):
                           "runs": runs, "l2": "512 MiB write before each run"}), flush=True)
 
 
+def run_chunking(args, rank, local):
+    """The chunking workload: 4096 samples of S = 256 (D = 3072), forward and
+    backward through the four calls, run as 1 x 4096, 2 x 2048, 16 x 256,
+    64 x 64 and 4096 x 1 chunks, dW/db accumulated in fp32 over the chunks.  One
+    JSON line per chunking on rank 0 (tokens/s over the whole workload, CUDA
+    events around it, W warm-up runs first); every chunking's dW equals the
+    first's bit for bit.  Inputs drawn on the device (seeded): x, dy, temb
+    ~ N(0, 1), W, b ~ N(0, 0.02^2), all rounded to bf16."""
+    if rank != 0:
+        return
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    build.build()
+    binding.load()
+    n, S, D = 4096, 256, 3072
+    N = 2 * D
+    g = torch.Generator(device="cuda")
+    g.manual_seed(WORKLOAD["seed"])
+    x = torch.randn((n, S, D), generator=g, device="cuda").to(torch.bfloat16)
+    dy = torch.randn((n, S, D), generator=g, device="cuda").to(torch.bfloat16)
+    temb = torch.randn((n, D), generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn((N, D), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    b = (torch.randn((N,), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    emb = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    u = torch.empty((n, D), dtype=torch.bfloat16, device="cuda")
+    out, dx = torch.empty_like(x), torch.empty_like(x)
+    mean = torch.empty((n, S), device="cuda")
+    rstd = torch.empty_like(mean)
+    d_emb = torch.empty((n, N), device="cuda")
+    d_temb = torch.empty_like(u)
+    accW = torch.empty((N, D), device="cuda")
+    accb = torch.empty((N,), device="cuda")
+    ws1 = torch.empty(binding.adaln_out_bwd_workspace_bytes(n, S, D), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty(binding.adaln_proj_bwd_workspace_bytes(n, D), dtype=torch.uint8, device="cuda")
+
+    def run(chunk):
+        for i in range(0, n, chunk):
+            j = i + chunk
+            binding.adaln_proj_fwd(temb[i:j], W, b, emb=emb[i:j], u=u[i:j])
+            binding.adaln_out_fwd(x[i:j], emb[i:j], out=out[i:j], mean=mean[i:j], rstd=rstd[i:j])
+            binding.adaln_out_bwd(dy[i:j], x[i:j], emb[i:j], mean[i:j], rstd[i:j], dx=dx[i:j], d_emb=d_emb[i:j],
+                                  workspace=ws1)
+            binding.adaln_proj_bwd(d_emb[i:j], temb[i:j], u[i:j], W, d_temb=d_temb[i:j], dW_acc=accW, db_acc=accb,
+                                   accumulate=i > 0, workspace=ws2)
+
+    ref = None
+    for chunk in (4096, 2048, 256, 64, 1):
+        for _ in range(max(1, min(args.warmup, 3))):
+            run(chunk)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run(chunk)
+        e1.record()
+        torch.cuda.synchronize()
+        if binding.device_error() != 0:
+            raise RuntimeError("device-side error in the chunking workload")
+        sec = e0.elapsed_time(e1) / 1e3
+        same = None
+        if ref is None:
+            ref = accW.clone()
+        else:
+            same = bool(torch.equal(accW.view(torch.int32), ref.view(torch.int32)))
+        print(json.dumps({"workload": "chunking: 4096 samples of S=256, D=3072, fwd+bwd", "chunks": n // chunk,
+                          "samples_per_chunk": chunk, "value": n * S / sec, "unit": "tokens/s", "ms": sec * 1e3,
+                          "dW_bitwise_equal_to_1x4096": same, "data": "synthetic (seeded, drawn on the device)"}),
+              flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -624,14 +919,21 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm's steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time the step as separate calls, not a CUDA graph")
+    ap.add_argument("--min-timed-s", type=float, default=1.5, help="repeat the K-step pass until this long is timed")
+    ap.add_argument("--max-passes", type=int, default=2000)
     ap.add_argument("--proj-sweep", action="store_true",
                     help="instead of the step: time the projection calls alone for B = 1 .. 2048")
+    ap.add_argument("--chunking", action="store_true",
+                    help="instead of the step: the 4096-sample chunking workload in its five chunkings")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
     if args.proj_sweep:
         run_proj_sweep(args, rank, local)
+        return
+    if args.chunking:
+        run_chunking(args, rank, local)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
