@@ -45,7 +45,8 @@
  *    B <= 2^20 for the projection calls; B * S * D < 2^40.  B == 0 or
  *    S == 0 is valid (see each call).
  *  - Nothing is thrown across the ABI; no global state changes except the
- *    device-side error word read by adaln_device_error().
+ *    device-side error words read by adaln_device_error() and the per-device
+ *    SiLU table filled once by the first adaln_proj_fwd.
  */
 #ifndef ADALN_H
 #define ADALN_H
@@ -149,12 +150,13 @@ size_t adaln_out_bwd_workspace_bytes(int B, int S, int D);
  *   g     = fp32(dy);  gh = g * onep (exact unless it underflows);  xhat as in
  *           the forward, from the saved mean/rstd, bit-identical to the
  *           forward's value
- *   dx    = bf16( rstd * ((gh - c1) - xhat * c2) ),  c1 = sum_d gh / D,
- *           c2 = sum_d gh*xhat / D   (fixed-order fp32 reductions over d, each
- *           sum times the correctly rounded 1/D).  The same quantity is
- *           evaluated as rstd*gh - rstd*c1 + (mean - x)*rstd^2*c2 with two
- *           fused multiply-adds, so dx is within the rounding error of this
- *           formula, not bit-identical to one fixed evaluation of it.
+ *   dx    = bf16( rstd * ((gh - c1) - xhat * c2) ),  c1 = sum_d g*onep / D,
+ *           c2 = sum_d fp32(g*xhat)*onep / D   (fixed-order fp32 reductions
+ *           over d, each sum times the correctly rounded 1/D).  The same
+ *           quantity is evaluated as rstd*gh + (mean*k2 - rstd*c1) - x*k2 with
+ *           k2 = rstd^2*c2, one multiply and two fused multiply-adds per
+ *           element, so dx is within the rounding error of this formula, not
+ *           bit-identical to one fixed evaluation of it.
  *   d_emb[b, 0:D]  = d_scale = tree_s( fp32(g * xhat) )
  *   d_emb[b, D:2D] = d_shift = tree_s( g )
  *
@@ -184,7 +186,9 @@ adaln_status adaln_out_bwd(const adaln_bf16 *dy, const adaln_bf16 *x, const adal
 
 /*
  * adaln_out_bwd_noalloc — adaln_out_bwd for callers that cannot allocate
- * device memory.  The pages have no counterpart of this call; it exists for
+ * device memory.  Arguments are checked as for adaln_out_bwd, in the same
+ * order (sizes, with the array's limit below counted as a size; NULL pointers;
+ * alignment; overlaps; then the device), and only then is the array looked up.  The pages have no counterpart of this call; it exists for
  * code that runs where allocation is not allowed: a plugin inside an engine
  * that owns all device memory and forbids allocations in its execute hook, a
  * real-time loop that must not take the allocator's locks or risk its
@@ -270,17 +274,53 @@ adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const ad
                             adaln_bf16 *dW, adaln_bf16 *db, int accumulate,
                             void *workspace, size_t workspace_bytes, int B, int D, void *stream);
 
+/*
+ * adaln_proj_wgrad_rows — the weight and bias gradient of adaln_proj_bwd for
+ * the output rows n0 <= n < n1 only, over B samples given in ascending order
+ * (the projection's dW/db, sharded by output rows: miles_diffusion PR 108,
+ * second rendering, "Patches": bitwise parity holds when no partial sums are
+ * reduced across GPUs, so a data-parallel step gathers the samples' d_emb and
+ * u, and each rank sums all samples for its own rows).
+ *
+ *   for n0 <= n < n1, with r = n - n0:
+ *     dW[r,k] : acc = accumulate ? dW_acc[r,k] : +0;
+ *               for b = 0 .. B-1 (ascending): acc = acc + e[b,n] * u[b,k]
+ *     db[r]   : the same with e[b,n] alone,      e = bf16(d_emb)
+ *
+ *   d_emb  [B, 2D]      fp32   input, every sample's (in the global order)
+ *   u      [B, D]       bf16   input, the same samples' SiLU activations
+ *   dW_acc [n1-n0, D]   fp32   in/out accumulator, or NULL
+ *   db_acc [n1-n0]      fp32   in/out accumulator, or NULL
+ *   dW     [n1-n0, D]   bf16   output bf16(acc), or NULL
+ *   db     [n1-n0]      bf16   output bf16(acc), or NULL
+ *
+ * The bytes equal rows n0..n1 of adaln_proj_bwd's results on the same samples
+ * (the same sequential fp32 order), so concatenating the row blocks of all
+ * ranks gives the one-GPU gradient.  0 <= n0 <= n1 <= 2D; no workspace.
+ */
+adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int n0, int n1, float *dW_acc,
+                                   float *db_acc, adaln_bf16 *dW, adaln_bf16 *db, int accumulate, int B, int D,
+                                   void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------ */
 
 /*
- * adaln_device_error — reads and clears the device-side error word of the
+ * adaln_device_error — reads and clears the device-side error words of the
  * current device (synchronizes the device).  Kernels that wait on their own
  * asynchronous copies give each wait a time limit; a wait that runs out sets
- * this word (non-zero: the kernel code) instead of hanging, and the kernel
- * returns without finishing its outputs.  Returns 0 when no kernel failed,
- * -1 if the word could not be read.
+ * a word instead of hanging, the kernel lets the copies it issued land, and it
+ * returns without finishing its outputs.  Codes: 0x101 adaln_out_fwd, 0x201
+ * adaln_out_bwd, 0x301 adaln_proj_fwd; bit 0x8000 is or-ed in when an issued
+ * copy did not land within the limit while the kernel was leaving.  Returns 0
+ * when no kernel failed, -1 if a word could not be read.
+ *
+ * Per-device state.  The library keeps, per device ordinal, the SiLU table's
+ * readiness, the address of adaln_out_bwd_noalloc's array and the kernels'
+ * shared-memory attributes.  cudaDeviceReset (or any other way of replacing a
+ * device's primary context) invalidates them: after it, the process must not
+ * call the library again on that device.
  */
 int adaln_device_error(void);
 

@@ -36,6 +36,7 @@ _SIGNATURES = {
     "token_sum_tree": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P]),
     "adaln_proj_bwd_workspace_bytes": (_SZ, [_I, _I]),
     "adaln_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _I, _I, _P]),
+    "adaln_proj_wgrad_rows": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P]),
     "adaln_device_error": (_I, []),
 }
 
@@ -262,3 +263,28 @@ def adaln_proj_bwd(d_emb, temb, u, W, d_temb=None, dW_acc=None, db_acc=None, dW=
                                               _ptr(dW_acc), _ptr(db_acc), _ptr(dW), _ptr(db), int(bool(accumulate)),
                                               _ptr(ws), nws, B, D, _stream(stream)))
     return d_temb, dW_acc, db_acc, dW, db
+
+
+def adaln_proj_wgrad_rows(d_emb, u, n0, n1, dW_acc=None, db_acc=None, dW=None, db=None, accumulate=False,
+                          stream=None):
+    """dW/db of the output rows n0 <= n < n1 over all given samples (ascending);
+    pass the row-block buffers you want ([n1-n0, D] and [n1-n0]).  Returns
+    (dW_acc, db_acc, dW, db) with None for those not computed."""
+    L = load()
+    B, D = u.shape
+    d_emb = _input(d_emb, torch.float32, (B, 2 * D), "d_emb")
+    u = _input(u, torch.bfloat16, (B, D), "u")
+    R = n1 - n0
+    dev = u.device
+    if dW_acc is not None:
+        dW_acc = _output(dW_acc, torch.float32, (R, D), "dW_acc", dev)
+    if db_acc is not None:
+        db_acc = _output(db_acc, torch.float32, (R,), "db_acc", dev)
+    if dW is not None:
+        dW = _output(dW, torch.bfloat16, (R, D), "dW", dev)
+    if db is not None:
+        db = _output(db, torch.bfloat16, (R,), "db", dev)
+    _check("adaln_proj_wgrad_rows", L.adaln_proj_wgrad_rows(_ptr(d_emb), _ptr(u), int(n0), int(n1), _ptr(dW_acc),
+                                                            _ptr(db_acc), _ptr(dW), _ptr(db), int(bool(accumulate)),
+                                                            B, D, _stream(stream)))
+    return dW_acc, db_acc, dW, db

@@ -277,6 +277,29 @@ adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const ad
                                      (cudaStream_t)stream, dev));
 }
 
+adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int n0, int n1, float *dW_acc,
+                                   float *db_acc, adaln_bf16 *dW, adaln_bf16 *db, int accumulate, int B, int D,
+                                   void *stream) {
+    if (!valid_D(D) || B < 0 || B > (1 << 20) || n0 < 0 || n1 < n0 || n1 > 2 * D) return ADALN_ERR_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return ADALN_ERR_ARG;
+    const bool want_w = dW_acc || dW, want_b = db_acc || db;
+    if (accumulate && ((want_w && !dW_acc) || (want_b && !db_acc))) return ADALN_ERR_ARG;
+    const size_t N = 2 * (size_t)D, R = (size_t)(n1 - n0);
+    const Buf ins[] = {{d_emb, (size_t)B * N * 4}, {u, (size_t)B * D * 2}};
+    const Buf outs[] = {{dW_acc, R * D * 4}, {db_acc, R * 4}, {dW, R * D * 2}, {db, R * 2}};
+    if (any_missing(ins, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(d_emb) || !aligned16(u) || !aligned16(dW_acc) || !aligned16(db_acc) || !aligned16(dW) ||
+        !aligned16(db))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 4, ins, 2)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (R == 0 || (!want_w && !want_b)) return ADALN_OK;
+    return from_cuda(launch_wgrad_rows(d_emb, u, n0, n1, dW_acc, db_acc, dW, db, accumulate, B, D,
+                                       (cudaStream_t)stream));
+}
+
 int adaln_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
     // the LayerNorm kernels' word first, then the projection kernels'; both cleared

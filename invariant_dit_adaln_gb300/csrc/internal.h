@@ -70,5 +70,7 @@ cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint
                             uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
                             int accumulate, void *ws, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
 int read_and_clear_proj_error();
+cudaError_t launch_wgrad_rows(const float *d_emb, const uint16_t *u, int n0, int n1, float *dW_acc, float *db_acc,
+                              uint16_t *dW, uint16_t *db, int accumulate, int B, int D, cudaStream_t stream);
 
 }  // namespace adaln

@@ -648,31 +648,33 @@ constexpr int kDwBChunk = 32;
 
 __global__ void __launch_bounds__(256)
 proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, float *__restrict__ dW_acc,
-                     uint16_t *__restrict__ dW, int accumulate, int B, int D) {
+                     uint16_t *__restrict__ dW, int accumulate, int B, int D, int n_begin, int nrows) {
+    // rows n_begin .. n_begin + nrows - 1 of the gradient; outputs indexed from that first row
     __shared__ __align__(16) float es[kDwBChunk][kDwTile];
     __shared__ __align__(16) float us[kDwBChunk][kDwTile];
     const int N = 2 * D;
     const int k0 = blockIdx.x * kDwTile;
-    const int n0 = blockIdx.y * kDwTile;
+    const int r0 = blockIdx.y * kDwTile;  // first output row of the tile, relative to n_begin
     const int tk = threadIdx.x & 15;
     const int tn = threadIdx.x >> 4;
     pdl_wait();
+    pdl_trigger();
     float acc[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-        const int n = n0 + 4 * tn + a;
+        const int r = r0 + 4 * tn + a;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int k = k0 + 4 * tk + c;
-            acc[a][c] = (accumulate && n < N && k < D) ? dW_acc[(size_t)n * D + k] : 0.0f;
+            acc[a][c] = (accumulate && r < nrows && k < D) ? dW_acc[(size_t)r * D + k] : 0.0f;
         }
     }
     for (int b0 = 0; b0 < B; b0 += kDwBChunk) {
         const int nb = min(kDwBChunk, B - b0);
         for (int i = threadIdx.x; i < kDwBChunk * kDwTile; i += blockDim.x) {
             const int b = i / kDwTile, j = i % kDwTile;
-            const int n = n0 + j, k = k0 + j;
-            es[b][j] = (b < nb && n < N) ? bf16f(bf16_bits(d_emb[(size_t)(b0 + b) * N + n])) : 0.0f;
+            const int r = r0 + j, k = k0 + j;
+            es[b][j] = (b < nb && r < nrows) ? bf16f(bf16_bits(d_emb[(size_t)(b0 + b) * N + n_begin + r])) : 0.0f;
             us[b][j] = (b < nb && k < D) ? bf16f(u[(size_t)(b0 + b) * D + k]) : 0.0f;
         }
         __syncthreads();
@@ -688,18 +690,17 @@ proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
         }
         __syncthreads();
     }
-    pdl_trigger();
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-        const int n = n0 + 4 * tn + a;
+        const int r = r0 + 4 * tn + a;
         const int k = k0 + 4 * tk;
-        if (n < N && k < D) {  // D % 8 == 0, so the 4 columns are all in range
-            if (dW_acc) stg16f(dW_acc + (size_t)n * D + k, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
+        if (r < nrows && k < D) {  // D % 8 == 0, so the 4 columns are all in range
+            if (dW_acc) stg16f(dW_acc + (size_t)r * D + k, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
             if (dW) {
                 uint2 p;
                 p.x = pack_bf16x2(acc[a][0], acc[a][1]);
                 p.y = pack_bf16x2(acc[a][2], acc[a][3]);
-                *reinterpret_cast<uint2 *>(dW + (size_t)n * D + k) = p;
+                *reinterpret_cast<uint2 *>(dW + (size_t)r * D + k) = p;
             }
         }
     }
@@ -707,16 +708,16 @@ proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
 
 __global__ void __launch_bounds__(256)
 proj_db_kernel(const float *__restrict__ d_emb, float *__restrict__ db_acc, uint16_t *__restrict__ db, int accumulate,
-               int B, int N) {
+               int B, int N, int n_begin, int nrows) {
     pdl_wait();
-    const int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n < N) {
-        float a = accumulate ? db_acc[n] : 0.0f;
-        for (int b = 0; b < B; ++b) a = __fadd_rn(a, bf16f(bf16_bits(d_emb[(size_t)b * N + n])));
-        if (db_acc) db_acc[n] = a;
-        if (db) db[n] = bf16_bits(a);
-    }
     pdl_trigger();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < nrows) {
+        float a = accumulate ? db_acc[r] : 0.0f;
+        for (int b = 0; b < B; ++b) a = __fadd_rn(a, bf16f(bf16_bits(d_emb[(size_t)b * N + n_begin + r])));
+        if (db_acc) db_acc[r] = a;
+        if (db) db[r] = bf16_bits(a);
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -833,6 +834,23 @@ static cudaError_t launch_slab_w(const float *d_emb, const uint16_t *u, const ui
     return launch_slab<BC, kSlabGeneral>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
 }
 
+// dW and db of the output rows [n0, n1) over all B samples (ascending), by the
+// tiled kernels; outputs indexed from row n0
+cudaError_t launch_wgrad_rows(const float *d_emb, const uint16_t *u, int n0, int n1, float *dW_acc, float *db_acc,
+                              uint16_t *dW, uint16_t *db, int accumulate, int B, int D, cudaStream_t stream) {
+    const int N = 2 * D;
+    const int nrows = n1 - n0;
+    cudaError_t err = cudaSuccess;
+    if (nrows <= 0) return err;
+    if (dW_acc || dW)
+        err = launch_pdl(proj_dw_tiled_kernel, dim3((D + kDwTile - 1) / kDwTile, (nrows + kDwTile - 1) / kDwTile),
+                         dim3(256), 0, stream, d_emb, u, dW_acc, dW, accumulate, B, D, n0, nrows);
+    if (err == cudaSuccess && (db_acc || db))
+        err = launch_pdl(proj_db_kernel, dim3((nrows + 255) / 256), dim3(256), 0, stream, d_emb, db_acc, db, accumulate,
+                         B, N, n0, nrows);
+    return err;
+}
+
 cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint16_t *u, const uint16_t *W,
                             uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
                             int accumulate, void *ws_v, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
@@ -847,12 +865,7 @@ cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint
         else err = launch_slab_w<4>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
     } else {
         err = launch_slab<4, kSlabDsOnly>(d_emb, u, W, nullptr, nullptr, nullptr, nullptr, 0, ws, B, D, stream, dev);
-        if (err == cudaSuccess && (dW_acc || dW))
-            err = launch_pdl(proj_dw_tiled_kernel, dim3((D + kDwTile - 1) / kDwTile, (N + kDwTile - 1) / kDwTile),
-                             dim3(256), 0, stream, d_emb, u, dW_acc, dW, accumulate, B, D);
-        if (err == cudaSuccess && (db_acc || db))
-            err = launch_pdl(proj_db_kernel, dim3((N + 255) / 256), dim3(256), 0, stream, d_emb, db_acc, db,
-                             accumulate, B, N);
+        if (err == cudaSuccess) err = launch_wgrad_rows(d_emb, u, 0, N, dW_acc, db_acc, dW, db, accumulate, B, D, stream);
     }
     if (err != cudaSuccess || B == 0) return err;
     const long long BD = (long long)B * D;

@@ -41,7 +41,7 @@ def fake(i, off=0):
 
 def test_library_exports_every_declared_symbol(L):
     names = binding.declared_symbols()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(L, n), n
     assert L.adaln_version() >> 16 == 1
@@ -196,6 +196,23 @@ def test_proj_bwd_checks(L, no_gpu):
     assert proj_bwd(L, db=fake(6, 16)) == ALIAS          # db inside db_acc
     assert proj_bwd(L, nws=8) == WORKSPACE
     assert proj_bwd(L, ws=None) == WORKSPACE
+
+
+def wgrad_rows(L, d_emb=0, u=1, n0=0, n1=100, dW_acc=2, db_acc=3, dW=4, db=5, acc=0, B=2, D=3072):
+    p = [None if a is None else (fake(a) if isinstance(a, int) else a) for a in (d_emb, u, dW_acc, db_acc, dW, db)]
+    return L.adaln_proj_wgrad_rows(p[0], p[1], n0, n1, p[2], p[3], p[4], p[5], acc, B, D, None)
+
+
+def test_proj_wgrad_rows_checks(L, no_gpu):
+    assert wgrad_rows(L, n1=6145) == SHAPE                 # beyond 2D rows
+    assert wgrad_rows(L, n0=10, n1=5) == SHAPE
+    assert wgrad_rows(L, n0=-1) == SHAPE
+    assert wgrad_rows(L, acc=3) == ARG
+    assert wgrad_rows(L, acc=1, dW_acc=None) == ARG
+    assert wgrad_rows(L, u=None) == NULL
+    assert wgrad_rows(L, dW=fake(4, 8)) == ALIGN
+    assert wgrad_rows(L, dW=fake(0, 64)) == ALIAS            # dW inside d_emb
+    assert wgrad_rows(L) == DEVICE                          # valid: the device check comes next
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="a valid call with fake pointers would launch on a GPU")

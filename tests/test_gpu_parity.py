@@ -297,3 +297,60 @@ def test_end_to_end_small_config():
     s_dW, s_db = oracle.wgrad_seq_f32(d_emb, inp["temb"])
     assert_bitwise(host_bf16(r["dW"]), synth.bf16_bits_from_f32(s_dW), "dW")
     assert_bitwise(host_bf16(r["db"]), synth.bf16_bits_from_f32(s_db), "db")
+
+
+@pytest.mark.parametrize("B,D", [(2, 3072), (6, 512), (3, 64)])
+def test_proj_wgrad_rows_equals_rows_of_proj_bwd(B, D):
+    """The row blocks of adaln_proj_wgrad_rows (the sharded step's weight
+    gradient), concatenated, are adaln_proj_bwd's dW and db bit for bit: with
+    one and with several samples per call, fp32 accumulators and bf16 outputs,
+    overwrite and accumulate."""
+    lib()
+    inp = synth.make_inputs(B, 1, D, 11)
+    temb, W = dev_bf16(inp["temb"]), dev_bf16(inp["W"])
+    N = 2 * D
+    d_emb = dev_f32(synth.normal(synth.stream_key(11, "aux"), B * N).astype(np.float32).reshape(B, N) * 2)
+    u = dev_bf16(oracle.silu_bf16(inp["temb"]))
+    acc0 = dev_f32(synth.normal(synth.stream_key(12, "aux"), N * D).astype(np.float32).reshape(N, D))
+    accb0 = dev_f32(synth.normal(synth.stream_key(13, "aux"), N).astype(np.float32))
+    for accumulate in (False, True):
+        refW = acc0.clone()
+        refb = accb0.clone()
+        dW = torch.empty((N, D), dtype=torch.bfloat16, device="cuda")
+        db = torch.empty((N,), dtype=torch.bfloat16, device="cuda")
+        binding.adaln_proj_bwd(d_emb, temb, u, W, dW_acc=refW, db_acc=refb, dW=dW, db=db, accumulate=accumulate)
+        cuts = [0, N // 3, N // 3 + 8, 2 * N // 3, N]
+        parts = []
+        for n0, n1 in zip(cuts[:-1], cuts[1:]):
+            a = acc0[n0:n1].clone()
+            ab = accb0[n0:n1].clone()
+            rW = torch.empty((n1 - n0, D), dtype=torch.bfloat16, device="cuda")
+            rb = torch.empty((n1 - n0,), dtype=torch.bfloat16, device="cuda")
+            binding.adaln_proj_wgrad_rows(d_emb, u, n0, n1, dW_acc=a, db_acc=ab, dW=rW, db=rb, accumulate=accumulate)
+            parts.append((a, ab, rW, rb))
+        torch.cuda.synchronize()
+        for i, (ref, name) in enumerate(((refW, "dW_acc"), (refb, "db_acc"), (dW, "dW"), (db, "db"))):
+            got = torch.cat([p[i] for p in parts])
+            assert_bitwise(host_f32(got) if got.dtype == torch.float32 else host_bf16(got),
+                           host_f32(ref) if ref.dtype == torch.float32 else host_bf16(ref), f"{name} acc={accumulate}")
+    assert binding.device_error() == 0
+
+
+def test_sharded_step_on_one_gpu_matches_the_step():
+    """The sharded step through the library with one rank (no exchange): its
+    per-sample results and its whole row block of dW, db are the plain step's
+    bytes."""
+    from invariant_dit_adaln_gb300 import sharded
+    from gpu_util import run_step
+    lib()
+    B, S, D = 3, 40, 512
+    inp = to_device(synth.make_inputs(B, S, D, 14, outlier_frac=0.05))
+    ref = run_step(inp)
+    plan = sharded.ShardPlan.make(B, D, 1, 0)
+    got = sharded.sharded_step(inp["x"], inp["dy"], inp["temb"], inp["W"], inp["b"], plan, dist=None)
+    torch.cuda.synchronize()
+    for k in ("emb", "u", "out", "mean", "rstd", "dx", "d_emb", "d_temb"):
+        assert torch.equal(got[k].view(torch.uint8), ref[k].view(torch.uint8)), k
+    assert torch.equal(got["dW_rows"].view(torch.int16), ref["dW"].view(torch.int16))
+    assert torch.equal(got["db_rows"].view(torch.int16), ref["db"].view(torch.int16))
+    assert binding.device_error() == 0
