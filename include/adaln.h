@@ -100,7 +100,12 @@ int adaln_version(void);
  *                         saved for adaln_proj_bwd)
  *
  * The k-order of every dot product is fixed by D alone, so emb[b,:] does not
- * depend on B or on b.  B == 0 launches nothing.
+ * depend on B or on b.  For D a multiple of 64 the sum runs on the tensor
+ * cores (tcgen05.mma, 128 rows of W x 32 samples x 16 k per instruction,
+ * fp32 accumulation in tensor memory): k is cut into a number of contiguous
+ * ranges fixed by D (3 for D = 3072), each range summed in ascending blocks
+ * of 16, and the ranges' partial sums are added in range order.  Other D use
+ * CUDA cores in one fixed order.  B == 0 launches nothing.
  *
  * The first call with B > 0 on a device also fills a 128 KB SiLU lookup table
  * in the library's device memory (a kernel on `stream`) and synchronizes
@@ -312,7 +317,8 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
  * asynchronous copies give each wait a time limit; a wait that runs out sets
  * a word instead of hanging, the kernel lets the copies it issued land, and it
  * returns without finishing its outputs.  Codes: 0x101 adaln_out_fwd, 0x201
- * adaln_out_bwd, 0x301 adaln_proj_fwd; bit 0x8000 is or-ed in when an issued
+ * adaln_out_bwd, 0x301 and 0x302 adaln_proj_fwd (CUDA-core and tensor-core
+ * kernels); bit 0x8000 is or-ed in when an issued
  * copy did not land within the limit while the kernel was leaving.  Returns 0
  * when no kernel failed, -1 if a word could not be read.
  *

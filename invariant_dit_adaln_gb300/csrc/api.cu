@@ -302,11 +302,12 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
 
 int adaln_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    // the LayerNorm kernels' word first, then the projection kernels'; both cleared
+    // the LayerNorm kernels' word first, then the projection kernels'; all cleared
     const int a = read_and_clear_device_error();
     const int b = read_and_clear_proj_error();
-    if (a < 0 || b < 0) return -1;
-    return a != 0 ? a : b;
+    const int c = read_and_clear_tc_error();
+    if (a < 0 || b < 0 || c < 0) return -1;
+    return a != 0 ? a : b != 0 ? b : c;
 }
 
 }  // extern "C"

@@ -28,6 +28,7 @@ enum DeviceError : unsigned {
     kErrOutFwdWait = 0x101,
     kErrOutBwdWait = 0x201,
     kErrProjFwdWait = 0x301,
+    kErrProjTcWait = 0x302,
     kErrDrainFailed = 0x8000,  // or-ed in: an issued copy did not land while leaving
 };
 
@@ -285,6 +286,20 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// The same without sleeping between tries: for a thread on the critical path
+// of a pipeline whose phases complete by asynchronous arrivals (TMA bytes,
+// tensor-core commits).
+__device__ __forceinline__ bool mbar_spin_or_abort(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                   uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

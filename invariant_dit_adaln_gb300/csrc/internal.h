@@ -70,6 +70,14 @@ cudaError_t launch_proj_bwd(const float *d_emb, const uint16_t *temb, const uint
                             uint16_t *d_temb, float *dW_acc, float *db_acc, uint16_t *dW, uint16_t *db,
                             int accumulate, void *ws, int B, int D, cudaStream_t stream, const DeviceInfo &dev);
 int read_and_clear_proj_error();
+
+// tc_proj.cu: emb = u W^T + bias on the tensor cores, for D a multiple of 64
+// (and a driver that provides the tensor-map encoder); u written beforehand.
+bool proj_fwd_tc_supported(int D);
+int proj_fwd_tc_ksplit(int D);
+cudaError_t launch_proj_fwd_tc(const uint16_t *u, const uint16_t *W, const uint16_t *bias, uint16_t *emb, int B,
+                               int D, cudaStream_t stream, const DeviceInfo &dev);
+int read_and_clear_tc_error();
 cudaError_t launch_wgrad_rows(const float *d_emb, const uint16_t *u, int n0, int n1, float *dW_acc, float *db_acc,
                               uint16_t *dW, uint16_t *db, int accumulate, int B, int D, cudaStream_t stream);
 

@@ -777,14 +777,22 @@ static cudaError_t launch_proj_fwd_wave(const uint16_t *temb, const uint16_t *W,
     return launch_pdl(kern, dim3(dev.sm_count), dim3(kWaveWarps * 32), smem, stream, temb, W, bias, emb, u, B, D);
 }
 
-// One or two samples with D <= 3072 (when every SM can hold its share of W):
-// the one-wave kernel.  Otherwise the SiLU kernel, then: up to kStreamMaxB
-// samples and D <= 3072, the streaming GEMV; otherwise the chunked GEMV.
+// D a multiple of 64: the SiLU kernel, then the tensor-core projection
+// (tc_proj.cu), for every B.  Other D (one order of the CUDA-core kernels for
+// every B): one or two samples with D <= 3072 (when every SM can hold its
+// share of W), the one-wave kernel; otherwise the SiLU kernel, then up to
+// kStreamMaxB samples and D <= 3072 the streaming GEMV, else the chunked GEMV.
 cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,
                             uint16_t *u, int B, int D, cudaStream_t stream, const DeviceInfo &dev) {
     if (B == 0) return cudaSuccess;
     cudaError_t err = ensure_silu_table(stream, dev);
     if (err != cudaSuccess) return err;
+    if (proj_fwd_tc_supported(D)) {
+        const long long n8 = (long long)B * D / 8;
+        err = launch_pdl(silu_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, stream, temb, u, n8);
+        if (err != cudaSuccess) return err;
+        return launch_proj_fwd_tc(u, W, bias, emb, B, D, stream, dev);
+    }
     if (B <= 2 && D / 8 <= 32 * kStreamVL && dev.sm_count > 0 && B * (D / 8) <= 2 * kWaveWarps * 32) {
         const int N = 2 * D;
         const int rows_max = (N + dev.sm_count - 1) / dev.sm_count;

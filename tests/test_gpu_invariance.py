@@ -64,16 +64,48 @@ def _one(dev, b):
 
 
 def test_projection_is_M_invariant_across_batch_sizes():
-    """emb rows are bit-identical for B = 1 .. 64, across the switch between
-    the fused streaming kernel (B <= 8) and the chunked kernel (B > 8)."""
+    """emb and u rows have the same bits for every B from 1 to 4096 and for
+    every position of a sample in the batch: the tensor-core tiles of 16
+    samples, a ragged last tile, the u box rounded up to 8 rows below 16
+    samples, one to 16 sample tiles per CTA and the stage layouts chosen by
+    batch size."""
     D = 3072
-    big = _device_inputs(64, 1, D, seed=3)
+    big = _device_inputs(4096, 1, D, seed=3)
     W, b = big["W"], big["b"]
     ref, uref = binding.adaln_proj_fwd(big["temb"], W, b)
-    for B in [1, 2, 3, 4, 5, 7, 8, 9, 16, 33]:
+    for B in [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 33, 64, 80, 81, 127, 128, 129, 255, 256, 257, 1000, 2048]:
         e, u = binding.adaln_proj_fwd(big["temb"][:B], W, b)
         assert torch.equal(_bits(e), _bits(ref[:B])), B
         assert torch.equal(_bits(u), _bits(uref[:B])), B
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    for n, start in [(300, 0), (129, 3000), (2, 4094)]:
+        idx = start + torch.randperm(n, generator=g, device="cuda")
+        e, u = binding.adaln_proj_fwd(big["temb"][idx].contiguous(), W, b)
+        assert torch.equal(_bits(e), _bits(ref[idx])), (n, start)
+        assert torch.equal(_bits(u), _bits(uref[idx])), (n, start)
+
+
+def test_projection_at_4096_samples_matches_the_oracle():
+    """Sampled samples of the 4096-sample projection (the first and last of
+    each tile of 128, and a few inside) against the oracle."""
+    import numpy as np
+    import oracle
+    from gpu_util import host_bf16
+    from tolerance import bf16_to_f64, check_bf16, floor_emb
+    oracle.build()
+    D = 3072
+    big = _device_inputs(4096, 1, D, seed=5)
+    emb, u = binding.adaln_proj_fwd(big["temb"], big["W"], big["b"])
+    rows = sorted({0, 1, 127, 128, 255, 2047, 2048, 3071, 4094, 4095, 1000, 1729})
+    temb = host_bf16(big["temb"])[rows]
+    W, bias = host_bf16(big["W"]), host_bf16(big["b"])
+    want = oracle.proj_fwd(temb, W, bias)
+    u_ref = oracle.silu_bf16(temb)
+    assert np.array_equal(host_bf16(u)[rows], u_ref)
+    fl = floor_emb(bf16_to_f64(u_ref), bf16_to_f64(W), bf16_to_f64(bias))
+    st = check_bf16(host_bf16(emb)[rows], want, fl, what="emb at B=4096")
+    assert st["exact"] >= 0.99 * st["n"], st
 
 
 @pytest.mark.parametrize("seed", [0, 127, 2026])
@@ -169,15 +201,17 @@ def _oracle_check_samples(dev, ref, refW, refb, samples, rows, D):
     import oracle
     from gpu_util import host_bf16, host_f32
     from tolerance import (assert_bitwise, bf16_to_f64, check_bf16, check_f32, check_rows, floor_d_emb,
-                           floor_d_temb)
+                           floor_d_temb, floor_emb)
     oracle.build()
     idx = torch.tensor(samples, device="cuda")
     h = {k: host_bf16(dev[k].index_select(0, idx)) for k in ("x", "dy", "temb")}
     W, b = host_bf16(dev["W"]), host_bf16(dev["b"])
     g = {k: (host_bf16(v.index_select(0, idx)) if v.dtype == torch.bfloat16 else host_f32(v.index_select(0, idx)))
          for k, v in ref.items()}
-    check_bf16(g["emb"], oracle.proj_fwd(h["temb"], W, b), what="1x4096 chunk: emb of sampled samples")
-    assert_bitwise(g["u"], oracle.silu_bf16(h["temb"]), "1x4096 chunk: u")
+    u_ref = oracle.silu_bf16(h["temb"])
+    check_bf16(g["emb"], oracle.proj_fwd(h["temb"], W, b), floor_emb(bf16_to_f64(u_ref), bf16_to_f64(W), bf16_to_f64(b)),
+               what="1x4096 chunk: emb of sampled samples")
+    assert_bitwise(g["u"], u_ref, "1x4096 chunk: u")
     check_rows(h["x"], h["dy"], g["emb"], g, oracle, what="1x4096 chunk: sampled samples")
     prod = oracle.bwd_products_f32(h["dy"], h["x"], g["mean"], g["rstd"])
     assert_bitwise(g["d_emb"], oracle.token_tree_f32(prod), "1x4096 chunk: d_emb vs the fp32 tree")

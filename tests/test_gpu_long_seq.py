@@ -17,7 +17,8 @@ import torch
 import oracle
 from invariant_dit_adaln_gb300 import binding, synth
 from gpu_util import host_bf16, host_f32, lib, run_step, to_device
-from tolerance import assert_bitwise, bf16_to_f64, check_bf16, check_f32, check_rows, floor_d_emb, floor_d_temb
+from tolerance import (assert_bitwise, bf16_to_f64, check_bf16, check_f32, check_rows, floor_d_emb, floor_d_temb,
+                       floor_emb)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,8 +39,10 @@ def run(request):
 
 def test_emb_and_u(run):
     S, inp, g = run
-    check_bf16(g["emb"], oracle.proj_fwd(inp["temb"], inp["W"], inp["b"]), what="emb")
-    assert_bitwise(g["u"], oracle.silu_bf16(inp["temb"]), "u")
+    u_ref = oracle.silu_bf16(inp["temb"])
+    fl = floor_emb(bf16_to_f64(u_ref), bf16_to_f64(inp["W"]), bf16_to_f64(inp["b"]))
+    check_bf16(g["emb"], oracle.proj_fwd(inp["temb"], inp["W"], inp["b"]), fl, what="emb")
+    assert_bitwise(g["u"], u_ref, "u")
 
 
 def test_out_and_dx_all_rows(run):

@@ -283,7 +283,8 @@ def test_end_to_end_small_config():
     r = run_step(to_device(inp))
     torch.cuda.synchronize()
     emb = host_bf16(r["emb"])
-    check_bf16(emb, oracle.proj_fwd(inp["temb"], inp["W"], inp["b"]), what="emb")
+    fl = floor_emb(bf16_to_f64(oracle.silu_bf16(inp["temb"])), bf16_to_f64(inp["W"]), bf16_to_f64(inp["b"]))
+    check_bf16(emb, oracle.proj_fwd(inp["temb"], inp["W"], inp["b"]), fl, what="emb")
     w_out, _, _ = oracle.out_fwd(inp["x"], emb)
     check_bf16(host_bf16(r["out"]), w_out, floor_out(bf16_to_f64(inp["x"]), *onep_shift(emb, 3072)), what="out")
     w_dx, w_demb = oracle.out_bwd(inp["dy"], inp["x"], emb)

@@ -5,9 +5,11 @@ that runs out sets the library's device error word and the kernel drains the
 copies it issued, then returns.  A test build of the library sends the first
 wait of every waiting kernel to an mbarrier that nothing ever arrives on (a
 200 us limit), so the path runs: the forward reports 0x101, the backward 0x201,
-no drain runs out (the 0x8000 bit stays clear), and the GPU context stays
-usable, shown by the release library's results afterwards being the same bytes
-as before.
+the tensor-core projection 0x302 (its MMA thread gives up, the TMA thread
+stops and lets its copies land, the cluster writes no emb and frees its tensor
+memory), no drain runs out (the 0x8000 bit stays clear), and the GPU context
+stays usable, shown by the release library's results afterwards being the same
+bytes as before.
 """
 
 from __future__ import annotations
@@ -22,7 +24,7 @@ from gpu_util import run_step, to_device
 
 pytestmark = pytest.mark.gpu
 
-FWD_WAIT, BWD_WAIT, DRAIN_FAILED = 0x101, 0x201, 0x8000
+FWD_WAIT, BWD_WAIT, PROJ_TC_WAIT, DRAIN_FAILED = 0x101, 0x201, 0x302, 0x8000
 
 
 @pytest.fixture(scope="module")
@@ -32,6 +34,7 @@ def wait_lib():
     P, I = ctypes.c_void_p, ctypes.c_int
     L.adaln_out_fwd.argtypes = [P, P, P, P, P, I, I, I, ctypes.c_float, P]
     L.adaln_out_bwd.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_size_t, I, I, I, P]
+    L.adaln_proj_fwd.argtypes = [P, P, P, P, P, I, I, P]
     L.adaln_device_error.restype = I
     return L
 
@@ -65,6 +68,12 @@ def test_waits_that_run_out_report_and_return(wait_lib, B, S, D):
                            B, S, D, st) == 0
     err = L.adaln_device_error()
     assert err & ~DRAIN_FAILED == BWD_WAIT and not err & DRAIN_FAILED, hex(err)
+    e2 = torch.empty_like(emb)
+    u2 = torch.empty_like(before["u"])
+    assert L.adaln_proj_fwd(inp["temb"].data_ptr(), inp["W"].data_ptr(), inp["b"].data_ptr(), e2.data_ptr(),
+                            u2.data_ptr(), B, D, st) == 0
+    err = L.adaln_device_error()
+    assert err & ~DRAIN_FAILED == PROJ_TC_WAIT and not err & DRAIN_FAILED, hex(err)
     assert L.adaln_device_error() == 0  # read and cleared
     # the context is still usable: the release library gives the same bytes
     after = run_step(inp)
