@@ -38,9 +38,9 @@ METRIC = "AdaLN-out fwd+bwd tokens/s and HBM GB/s (% of 8 TB/s) at B=2,S=4096,D=
 WORKLOAD = dict(B=2, S=4096, D=3072, seed=0, outlier_frac=0.01)
 NOMINAL_HBM_GBS = 8000.0
 FLUSH_BYTES = 512 << 20
-# kernels per step at this workload: projection, LayerNorm forward, backward
-# tile, tree fold, projection-backward slab, d_temb
-KERNELS_PER_STEP = 6
+# kernels per step at this workload: SiLU, tensor-core projection, LayerNorm
+# forward, backward tile, tree fold, projection-backward slab, d_temb
+KERNELS_PER_STEP = 7
 # DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold)
 # at this workload, from one ncu capture of the current kernels (dram__bytes_read.sum
 # + dram__bytes_write.sum); None when the kernels changed after the capture.
@@ -697,7 +697,7 @@ def run_gpu(args, world, rank, local):
         "config": {"workload": "AdaLN norm_out fwd+bwd, B=2 S=4096 D=3072, 1% outlier rows",
                    "B": B, "S": S, "D": D, "parallelism": "replicas" if world > 1 else "single GPU",
                    "launch": ("eager: one C-ABI call at a time" if graphs is None else
-                              "CUDA graphs of the step's four C-ABI calls (6 kernels, programmatic launch edges), "
+                              "CUDA graphs of the step's four C-ABI calls (7 kernels, programmatic launch edges), "
                               "one per input set, captured once after the warm-up; K steps replayed back to back"),
                    "l2": ("inputs larger than L2: consecutive steps alternate between two copies of the inputs "
                           "(138 MB each, L2 129 MB), no flush; ms_per_step_flushed: the same step with a 512 MiB "
