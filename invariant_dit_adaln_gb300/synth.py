@@ -34,7 +34,8 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # Tensor identifiers folded into the stream keys.
-TENSOR_IDS = {"x": 1, "temb": 2, "W": 3, "b": 4, "dy": 5, "outlier": 6, "aux": 7}
+TENSOR_IDS = {"x": 1, "temb": 2, "W": 3, "b": 4, "dy": 5, "outlier": 6, "aux": 7, "residual": 8, "gate": 9,
+              "emb": 10, "dr": 11}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -155,6 +156,32 @@ def make_inputs(B: int, S: int, D: int = 3072, seed: int = 0, sample0: int = 0,
         "temb": temb.reshape(B, D),
         "W": normal_bf16(stream_key(seed, "W"), 2 * D * D, std=w_std).reshape(2 * D, D),
         "b": normal_bf16(stream_key(seed, "b"), 2 * D, std=w_std),
+        "outlier_rows": rows if rows is not None else np.zeros(0, dtype=np.int64),
+    }
+
+
+def make_block_inputs(B: int, S: int, D: int = 3072, seed: int = 0, sample0: int = 0,
+                      outlier_frac: float = 0.0) -> dict:
+    """Inputs of the block-level modulated norm with a gated residual, as
+    bfloat16 bits: x (the branch output), residual and dy (the gradient of the
+    norm's output) [B, S, D] ~ N(0, 1), dr (the residual output's gradient
+    from later uses) [B, S, D] ~ N(0, 1); gate [B, D] ~ N(0, 0.5^2) and emb =
+    [scale | shift] [B, 2D] ~ N(0, 0.3^2), drawn per sample like temb.  The
+    same outlier rows (x50) in x, residual, dy and dr."""
+    rows = outlier_rows(seed, B, S, outlier_frac) if outlier_frac > 0 else None
+
+    def per_sample(tensor, n, std):
+        if B == 0:
+            return np.zeros((0, n), dtype=np.uint16)
+        return np.stack([normal_bf16(stream_key(seed, tensor, sample0 + b), n, std=std) for b in range(B)])
+
+    return {
+        "x": token_tensor(seed, "x", B, S, D, sample0, rows),
+        "residual": token_tensor(seed, "residual", B, S, D, sample0, rows),
+        "dy": token_tensor(seed, "dy", B, S, D, sample0, rows),
+        "dr": token_tensor(seed, "dr", B, S, D, sample0, rows),
+        "gate": per_sample("gate", D, 0.5).reshape(B, D),
+        "emb": per_sample("emb", 2 * D, 0.3).reshape(B, 2 * D),
         "outlier_rows": rows if rows is not None else np.zeros(0, dtype=np.int64),
     }
 

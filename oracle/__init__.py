@@ -65,6 +65,10 @@ def _load():
             "oracle_wgrad_seq_f32": [P, P, P, P, I, I, I],
             "oracle_wgrad_seq_f32_rows": [P, P, P, I, P, P, I, I],
             "oracle_bf16_from_f64": [P, P, Lg],
+            "oracle_res_fwd": [P, P, P, P, F, P, P, P, P, I, I, I],
+            "oracle_res_bwd_tail": [P, P, P, P, P, P, P, I, I, I],
+            "oracle_res_bwd": [P, P, P, P, P, P, F, P, P, P, P, I, I, I],
+            "oracle_res_gate_products_f32": [P, P, P, Lg],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -259,6 +263,62 @@ def wgrad_seq_f32_rows(d_emb, temb, rows):
     db = np.empty(len(rows), np.float32)
     _load().oracle_wgrad_seq_f32_rows(_p(d_emb), _p(temb), _p(rows), len(rows), _p(dW), _p(db), B, D)
     return dW, db
+
+
+# --- block-level modulated norm with a gated residual ----------------------
+
+def res_fwd(x, residual, gate, emb, eps=EPS):
+    """(r, out, mean, rstd): r = bf16(residual + bf16(gate * x)), then the
+    LayerNorm + modulation of r."""
+    x, residual = _c(x, np.uint16), _c(residual, np.uint16)
+    gate, emb = _c(gate, np.uint16), _c(emb, np.uint16)
+    B, S, D = x.shape
+    assert residual.shape == x.shape and gate.shape == (B, D) and emb.shape == (B, 2 * D)
+    r = np.empty_like(x)
+    out = np.empty_like(x)
+    mean = np.empty((B, S), dtype=np.float32)
+    rstd = np.empty((B, S), dtype=np.float32)
+    _load().oracle_res_fwd(_p(x), _p(residual), _p(gate), _p(emb), float(eps), _p(r), _p(out), _p(mean),
+                           _p(rstd), B, S, D)
+    return r, out, mean, rstd
+
+
+def res_bwd_tail(dr_ln, d_r, x, gate):
+    """(d_x, d_residual, d_gate) from the LayerNorm input's gradient dr_ln
+    (bf16) and the residual output's gradient d_r (bf16, or None)."""
+    dr_ln, x, gate = _c(dr_ln, np.uint16), _c(x, np.uint16), _c(gate, np.uint16)
+    B, S, D = x.shape
+    dr = None if d_r is None else _c(d_r, np.uint16)
+    d_x = np.empty_like(x)
+    d_res = np.empty_like(x)
+    d_gate = np.empty((B, D), dtype=np.float32)
+    _load().oracle_res_bwd_tail(_p(dr_ln), None if dr is None else _p(dr), _p(x), _p(gate), _p(d_x), _p(d_res),
+                                _p(d_gate), B, S, D)
+    return d_x, d_res, d_gate
+
+
+def res_bwd(d_out, d_r, x, r, gate, emb, eps=EPS):
+    """(d_x, d_residual, d_emb, d_gate): the whole backward of res_fwd."""
+    d_out, x, r = _c(d_out, np.uint16), _c(x, np.uint16), _c(r, np.uint16)
+    gate, emb = _c(gate, np.uint16), _c(emb, np.uint16)
+    B, S, D = x.shape
+    dr = None if d_r is None else _c(d_r, np.uint16)
+    d_x = np.empty_like(x)
+    d_res = np.empty_like(x)
+    d_emb = np.empty((B, 2 * D), dtype=np.float32)
+    d_gate = np.empty((B, D), dtype=np.float32)
+    _load().oracle_res_bwd(_p(d_out), None if dr is None else _p(dr), _p(x), _p(r), _p(gate), _p(emb), float(eps),
+                           _p(d_x), _p(d_res), _p(d_emb), _p(d_gate), B, S, D)
+    return d_x, d_res, d_emb, d_gate
+
+
+def res_gate_products_f32(gr, x):
+    """bf16(gr * x) as fp32: the token products of d_gate."""
+    gr, x = _c(gr, np.uint16), _c(x, np.uint16)
+    assert gr.shape == x.shape
+    prod = np.empty(x.shape, dtype=np.float32)
+    _load().oracle_res_gate_products_f32(_p(gr), _p(x), _p(prod), x.size)
+    return prod
 
 
 def bf16_from_f64(a):

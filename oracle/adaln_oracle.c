@@ -585,6 +585,78 @@ void oracle_wgrad_seq_f32_rows(const float *d_emb, const uint16_t *temb, const i
 }
 
 /* ------------------------------------------------------------------------ */
+/* Block-level modulated norm with a gated residual                           */
+/* (ScaleResidualLayerNormScaleShift: miles_diffusion PR 108, Summary, root   */
+/* cause 1 and "Patches": the norm1/norm2 sites of every block take the same  */
+/* rounding points as norm_out -- fp32 LayerNorm, bf16 (1 + scale), fp32      */
+/* modulation -- with the residual stream's gated add in eager bf16, each op  */
+/* computed in fp32 and rounded once to bf16)                                 */
+/* ------------------------------------------------------------------------ */
+
+/* eager bf16 multiply and add: fp32 operation, one rounding to bf16 */
+static uint16_t bf16_mul(uint16_t a, uint16_t b) { return bf16_from_f32(bf16_to_f32(a) * bf16_to_f32(b)); }
+static uint16_t bf16_add(uint16_t a, uint16_t b) { return bf16_from_f32(bf16_to_f32(a) + bf16_to_f32(b)); }
+
+/* r = bf16(residual + bf16(gate * x)), gate [B, D] broadcast over tokens;
+ * then out, mean, rstd = LayerNorm + modulation of r (oracle_out_fwd).      */
+void oracle_res_fwd(const uint16_t *x, const uint16_t *residual, const uint16_t *gate, const uint16_t *emb,
+                    float eps, uint16_t *r, uint16_t *out, float *mean, float *rstd, int B, int S, int D)
+{
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s)
+            for (int d = 0; d < D; ++d) {
+                size_t i = ((size_t)b * S + s) * D + d;
+                r[i] = bf16_add(residual[i], bf16_mul(gate[(size_t)b * D + d], x[i]));
+            }
+    oracle_out_fwd(r, emb, eps, out, mean, rstd, B, S, D);
+}
+
+/* The backward's tail from the LayerNorm input's gradient dr_ln (bf16, the
+ * dx of the norm_out backward applied to r) and the gradient d_r of the
+ * residual output from later uses (NULL: none):
+ *   gr         = bf16(dr_ln + d_r)           (autograd adds the two uses)
+ *   d_residual = gr
+ *   d_x        = bf16(gr * gate)
+ *   d_gate     = sum_s bf16(gr * x)          (the broadcast operand's grad,
+ *                                             products in eager bf16), fp32  */
+void oracle_res_bwd_tail(const uint16_t *dr_ln, const uint16_t *d_r, const uint16_t *x, const uint16_t *gate,
+                         uint16_t *d_x, uint16_t *d_residual, float *d_gate, int B, int S, int D)
+{
+    nsum *acc = malloc(sizeof(nsum) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) acc[d].s = acc[d].c = 0.0;
+        for (int s = 0; s < S; ++s)
+            for (int d = 0; d < D; ++d) {
+                size_t i = ((size_t)b * S + s) * D + d;
+                uint16_t gr = d_r ? bf16_add(dr_ln[i], d_r[i]) : dr_ln[i];
+                d_residual[i] = gr;
+                d_x[i] = bf16_mul(gr, gate[(size_t)b * D + d]);
+                nsum_add(&acc[d], bf16_to_f64(bf16_mul(gr, x[i])));
+            }
+        for (int d = 0; d < D; ++d) d_gate[(size_t)b * D + d] = (float)nsum_val(&acc[d]);
+    }
+    free(acc);
+}
+
+/* the whole backward of oracle_res_fwd: dr_ln, d_emb from oracle_out_bwd on r */
+void oracle_res_bwd(const uint16_t *d_out, const uint16_t *d_r, const uint16_t *x, const uint16_t *r,
+                    const uint16_t *gate, const uint16_t *emb, float eps, uint16_t *d_x, uint16_t *d_residual,
+                    float *d_emb, float *d_gate, int B, int S, int D)
+{
+    uint16_t *dr_ln = malloc(sizeof(uint16_t) * (size_t)B * S * D);
+    oracle_out_bwd(d_out, r, emb, eps, dr_ln, d_emb, B, S, D);
+    oracle_res_bwd_tail(dr_ln, d_r, x, gate, d_x, d_residual, d_gate, B, S, D);
+    free(dr_ln);
+}
+
+/* the gate's token products bf16(gr * x) as fp32, the input of the fixed
+ * token tree that replays d_gate (oracle_token_tree_f32)                     */
+void oracle_res_gate_products_f32(const uint16_t *gr, const uint16_t *x, float *prod, long n)
+{
+    for (long i = 0; i < n; ++i) prod[i] = bf16_to_f32(bf16_mul(gr[i], x[i]));
+}
+
+/* ------------------------------------------------------------------------ */
 /* format helpers exported for the tests                                     */
 /* ------------------------------------------------------------------------ */
 

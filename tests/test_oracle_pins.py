@@ -622,3 +622,111 @@ def test_wgrad_seq_f32_rows(orc):
     got, gotb = orc.wgrad_seq_f32_rows(d_emb, temb, rows)
     assert_bitwise(got, full[rows], "rows of the full accumulation")
     assert_bitwise(gotb, fullb[rows], "rows of db")
+
+
+# ---------------------------------------------------------------------------
+# block-level modulated norm with a gated residual (ScaleResidualLayerNorm-
+# ScaleShift; miles_diffusion PR 108 Summary, root cause 1)
+# ---------------------------------------------------------------------------
+
+def _block(B, S, D, seed):
+    return synth.make_block_inputs(B, S, D, seed)
+
+
+def _tbf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def _bits_of(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_res_fwd_residual_is_eager_bf16(orc):
+    """r = residual + gate * x in eager bf16: against PyTorch's bf16 ops on the
+    CPU and against exact rationals rounded twice (after the product and after
+    the sum); out, mean, rstd are the norm_out forward of r."""
+    B, S, D = 2, 7, 40
+    i = _block(B, S, D, 3)
+    r, out, mean, rstd = orc.res_fwd(i["x"], i["residual"], i["gate"], i["emb"])
+    t = _tbf16(i["residual"]) + _tbf16(i["gate"])[:, None, :] * _tbf16(i["x"])
+    assert_bitwise(r, _bits_of(t), "r vs torch bf16")
+    xf, rf, gf = bf16_to_f64(i["x"]), bf16_to_f64(i["residual"]), bf16_to_f64(i["gate"])
+    one_rounding_differs = 0
+    for b in range(B):
+        for s in range(S):
+            for d in range(D):
+                p = Fraction(float(gf[b, d])) * Fraction(float(xf[b, s, d]))
+                h = bf16_exact_round(p)
+                hv = Fraction(float(bf16_to_f64(np.array([h], np.uint16))[0]))
+                want = bf16_exact_round(Fraction(float(rf[b, s, d])) + hv)
+                assert int(r[b, s, d]) == want, (b, s, d)
+                one_rounding_differs += bf16_exact_round(Fraction(float(rf[b, s, d])) + p) != want
+    # the product's own rounding matters on these inputs: a fused form would fail
+    assert one_rounding_differs > 0
+    w_out, w_mean, w_rstd = orc.out_fwd(r, i["emb"])
+    assert_bitwise(out, w_out, "out")
+    assert_bitwise(mean, w_mean, "mean")
+    assert_bitwise(rstd, w_rstd, "rstd")
+
+
+def test_res_fwd_special_cases(orc):
+    """gate = 0 gives r = residual; residual = 0 gives r = bf16(gate * x);
+    gate = 1 gives r = bf16(residual + x)."""
+    B, S, D = 1, 5, 24
+    i = _block(B, S, D, 4)
+    one = np.full((B, D), 0x3F80, np.uint16)
+    r0, _, _, _ = orc.res_fwd(i["x"], i["residual"], np.zeros((B, D), np.uint16), i["emb"])
+    assert_bitwise(r0, i["residual"], "gate 0")
+    r1, _, _, _ = orc.res_fwd(i["x"], np.zeros_like(i["x"]), i["gate"], i["emb"])
+    assert_bitwise(r1, _bits_of(_tbf16(i["gate"])[:, None, :] * _tbf16(i["x"])), "residual 0")
+    r2, _, _, _ = orc.res_fwd(i["x"], i["residual"], one, i["emb"])
+    assert_bitwise(r2, _bits_of(_tbf16(i["residual"]) + _tbf16(i["x"])), "gate 1")
+
+
+def test_res_bwd_tail_matches_torch_autograd_in_bf16(orc):
+    """d_residual, d_x: the bf16 autograd of r = residual + gate * x (PyTorch
+    on the CPU, bf16 tensors) given the gradient of r as the bf16 sum of its
+    two uses; d_gate: the exact sum over tokens of the bf16 products gr * x
+    (math.fsum), rounded once to fp32."""
+    B, S, D = 2, 9, 32
+    i = _block(B, S, D, 5)
+    dr_ln = i["dy"]
+    d_x, d_res, d_gate = orc.res_bwd_tail(dr_ln, i["dr"], i["x"], i["gate"])
+    x = _tbf16(i["x"]).clone().requires_grad_(True)
+    res = _tbf16(i["residual"]).clone().requires_grad_(True)
+    gate = _tbf16(i["gate"])[:, None, :].clone().requires_grad_(True)
+    r = res + gate * x
+    gr = _tbf16(dr_ln) + _tbf16(i["dr"])
+    r.backward(gr)
+    assert_bitwise(d_res, _bits_of(res.grad), "d_residual")
+    assert_bitwise(d_x, _bits_of(x.grad), "d_x")
+    prod = bf16_to_f64(_bits_of(gr * _tbf16(i["x"])))
+    want = np.array([[math.fsum(prod[b, :, d]) for d in range(D)] for b in range(B)]).astype(np.float32)
+    assert_bitwise(d_gate, want, "d_gate")
+    # without the later use, gr is dr_ln itself
+    d_x0, d_res0, _ = orc.res_bwd_tail(dr_ln, None, i["x"], i["gate"])
+    assert_bitwise(d_res0, dr_ln, "d_residual without d_r")
+    assert_bitwise(d_x0, _bits_of(_tbf16(dr_ln) * _tbf16(i["gate"])[:, None, :]), "d_x without d_r")
+
+
+def test_res_bwd_is_the_norm_backward_then_the_tail(orc):
+    """The whole backward: d_emb and the LayerNorm input's gradient from the
+    norm_out backward applied to r, then the tail; the gate products replayed
+    by the fixed token tree stay within the tree's error bound of d_gate."""
+    B, S, D = 2, 37, 24
+    i = _block(B, S, D, 6)
+    r, _, _, _ = orc.res_fwd(i["x"], i["residual"], i["gate"], i["emb"])
+    d_x, d_res, d_emb, d_gate = orc.res_bwd(i["dy"], i["dr"], i["x"], r, i["gate"], i["emb"])
+    dr_ln, w_demb = orc.out_bwd(i["dy"], r, i["emb"])
+    assert_bitwise(d_emb, w_demb, "d_emb")
+    w_dx, w_dres, w_dgate = orc.res_bwd_tail(dr_ln, i["dr"], i["x"], i["gate"])
+    assert_bitwise(d_x, w_dx, "d_x")
+    assert_bitwise(d_res, w_dres, "d_residual")
+    assert_bitwise(d_gate, w_dgate, "d_gate")
+    prod = orc.res_gate_products_f32(d_res, i["x"])
+    assert_bitwise(prod, bf16_to_f64(_bits_of(_tbf16(d_res) * _tbf16(i["x"]))).astype(np.float32), "products")
+    tree = orc.token_tree_f32(prod)
+    exact = np.array([[math.fsum(prod[b, :, d].astype(np.float64)) for d in range(D)] for b in range(B)])
+    bound = 2.0 ** -23 * np.abs(exact) + 2.0 ** -30 * np.abs(prod).astype(np.float64).sum(axis=1)
+    assert np.all(np.abs(tree - exact) <= bound + 2.0 ** -24 * np.abs(exact))
+    assert np.all(np.abs(d_gate.astype(np.float64) - exact) <= 2.0 ** -24 * np.abs(exact))
