@@ -666,14 +666,7 @@ def run_gpu(args, world, rank, local):
     value = throughput(tokens * K, world, t_max)
     sbytes = step_bytes(B, S, D)
     gbs = sbytes * K / my_time / 1e9
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    peak, peak_src = hbm_peak()
     cb = call_bytes(B, S, D)
     dom = "adaln_out_bwd"
     ach = cb[dom] / (call_ms[dom] / 1e3) / 1e9
@@ -909,6 +902,98 @@ def run_chunking(args, rank, local):
               flush=True)
 
 
+def hbm_peak():
+    """(GB/s, source): the measured copy bandwidth of MEASURED_PEAKS.json, else
+    the machine's fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        if "hbm_gbs" in peaks:
+            return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, ValueError):
+        pass
+    return 6800.0, "fallback"
+
+
+def run_block(args, rank, local):
+    """The block-level modulated norm with a gated residual
+    (adaln_scale_residual_norm_fwd + _bwd with the residual output's later
+    gradient) at B=2, S=4096, D=3072: K steps replayed from a CUDA graph, two
+    input sets larger than L2 alternating, median of passes; one JSON line on
+    rank 0 with tokens/s and the algorithmic HBM bytes of the pair (forward:
+    x, residual read, r, out written, mean/rstd; backward: d_out, d_r, x, r
+    read, d_x, d_residual written, stats), against the measured copy peak."""
+    if rank != 0:
+        return
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    build.build()
+    binding.load()
+    B, S, D = 2, 4096, 3072
+    g = torch.Generator(device="cuda")
+    g.manual_seed(WORKLOAD["seed"])
+
+    def make():
+        t = {k: torch.randn((B, S, D), generator=g, device="cuda").to(torch.bfloat16)
+             for k in ("x", "residual", "dy", "dr")}
+        t["gate"] = (torch.randn((B, D), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+        t["emb"] = (torch.randn((B, 2 * D), generator=g, device="cuda") * 0.3).to(torch.bfloat16)
+        for k in ("r", "out", "d_x", "d_res"):
+            t[k] = torch.empty((B, S, D), dtype=torch.bfloat16, device="cuda")
+        t["mean"], t["rstd"] = torch.empty((B, S), device="cuda"), torch.empty((B, S), device="cuda")
+        t["d_emb"], t["d_gate"] = torch.empty((B, 2 * D), device="cuda"), torch.empty((B, D), device="cuda")
+        t["ws"] = torch.empty(binding.adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D), dtype=torch.uint8,
+                              device="cuda")
+        return t
+
+    sets = [make(), make()]
+    stream = torch.cuda.Stream()
+
+    def step(t):
+        binding.adaln_scale_residual_norm_fwd(t["x"], t["residual"], t["gate"], t["emb"], r=t["r"], out=t["out"],
+                                              mean=t["mean"], rstd=t["rstd"], stream=stream)
+        binding.adaln_scale_residual_norm_bwd(t["dy"], t["dr"], t["x"], t["r"], t["gate"], t["emb"], t["mean"],
+                                              t["rstd"], d_x=t["d_x"], d_residual=t["d_res"], d_emb=t["d_emb"],
+                                              d_gate=t["d_gate"], workspace=t["ws"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for t in sets:
+                step(t)
+    torch.cuda.synchronize()
+    graphs = []
+    for t in sets:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(t)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+    K = min(args.steps, 2000)
+    passes = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            graphs[i % 2].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        passes.append(e0.elapsed_time(e1) / K)
+    if binding.device_error() != 0:
+        raise RuntimeError("device-side error in the block-norm workload")
+    ms = statistics.median(passes)
+    alg = B * S * (4 * 2 * D + 8) + B * S * (6 * 2 * D + 8) + 4 * B * D * 2
+    peak, peak_src = hbm_peak()
+    print(json.dumps({"workload": "block-level modulated norm with a gated residual, fwd+bwd, B=2 S=4096 D=3072",
+                      "value": B * S / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+                      "algorithmic_bytes_per_step": alg, "hbm_gbs": alg / (ms / 1e3) / 1e9,
+                      "hbm_frac": alg / (ms / 1e3) / 1e9 / peak, "peak_gbs": peak, "peak_source": peak_src,
+                      "kernels_per_step": 6, "steps_per_pass": K, "passes": len(passes),
+                      "l2": "two input sets alternate (each: four 50.3 MB token inputs and four 50.3 MB token outputs, more than L2); no flush",
+                      "data": "synthetic (seeded, drawn on the device)"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -925,6 +1010,8 @@ def main(argv=None):
                     help="instead of the step: time the projection calls alone for B = 1 .. 2048")
     ap.add_argument("--chunking", action="store_true",
                     help="instead of the step: the 4096-sample chunking workload in its five chunkings")
+    ap.add_argument("--block", action="store_true",
+                    help="instead of the step: the block-level modulated norm with a gated residual, fwd+bwd")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -934,6 +1021,9 @@ def main(argv=None):
         return
     if args.chunking:
         run_chunking(args, rank, local)
+        return
+    if args.block:
+        run_block(args, rank, local)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)

@@ -308,6 +308,74 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
                                    void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Block-level modulated norm with a gated residual                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * adaln_scale_residual_norm_fwd — ScaleResidualLayerNormScaleShift, the
+ * norm1/norm2 site of every transformer block, with the final norm's rounding
+ * points (miles_diffusion PR 108, Summary, root cause 1, and "Patches": fp32
+ * LayerNorm, (1 + scale) rounded once to bf16, fp32 modulation; the residual
+ * stream's gated add in eager bf16, each operation computed in fp32 and
+ * rounded once to bf16).
+ *
+ *   r[b,s,d]  = bf16( residual[b,s,d] + bf16(gate[b,d] * x[b,s,d]) )
+ *   out, mean, rstd = adaln_out_fwd(r, emb)   (the same formulas and orders)
+ *
+ *   x        [B, S, D] bf16   the branch output (attention or MLP)
+ *   residual [B, S, D] bf16   the residual stream
+ *   gate     [B, D]    bf16   per-sample gate, broadcast over tokens
+ *   emb      [B, 2D]   bf16   [scale | shift] of the block's modulation
+ *   r        [B, S, D] bf16   output: the new residual stream (also the
+ *                             LayerNorm's input, saved for the backward)
+ *   out      [B, S, D] bf16   output
+ *   mean, rstd [B, S]  fp32   output, saved for the backward
+ *
+ * The plain LayerNormScaleShift (no residual) is adaln_out_fwd with the
+ * block's [scale | shift] as emb.  Rows never interact.  B * S == 0 launches
+ * nothing.  Errors as adaln_out_fwd.
+ */
+adaln_status adaln_scale_residual_norm_fwd(const adaln_bf16 *x, const adaln_bf16 *residual, const adaln_bf16 *gate,
+                                           const adaln_bf16 *emb, adaln_bf16 *r, adaln_bf16 *out, float *mean,
+                                           float *rstd, int B, int S, int D, float eps, void *stream);
+
+/* Workspace bytes adaln_scale_residual_norm_bwd needs (the tree nodes of
+ * d_scale, d_shift and then of d_gate, in the same space): the same as
+ * adaln_out_bwd_workspace_bytes(B, S, D). */
+size_t adaln_scale_residual_norm_bwd_workspace_bytes(int B, int S, int D);
+
+/*
+ * adaln_scale_residual_norm_bwd — backward of adaln_scale_residual_norm_fwd
+ * (autograd of the same graph, with the token sums of the broadcast
+ * operands by the fixed 32-way tree of RL-Kernel PR 538 "What").
+ *
+ *   dr_ln, d_emb = adaln_out_bwd(d_out, r, emb, mean, rstd)
+ *   gr[b,s,d]    = bf16(dr_ln + d_r)       (r's two uses; dr_ln if d_r is NULL)
+ *   d_residual   = gr
+ *   d_x          = bf16(gr * gate)
+ *   d_gate[b,d]  = sum over s of bf16(gr * x), fp32, by the token tree
+ *
+ *   d_out      [B, S, D] bf16   input: the gradient of out
+ *   d_r        [B, S, D] bf16   input: the gradient of r from its later uses,
+ *                               or NULL (none)
+ *   x, r, gate, emb, mean, rstd  inputs as saved by the forward
+ *   d_x        [B, S, D] bf16   output
+ *   d_residual [B, S, D] bf16   output (it holds dr_ln between the kernels)
+ *   d_emb      [B, 2D]   fp32   output [d_scale | d_shift]
+ *   d_gate     [B, D]    fp32   output
+ *   workspace  >= adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D)
+ *
+ * Every per-sample output of sample b depends only on sample b.  S == 0
+ * writes zero d_emb and d_gate; B == 0 launches nothing.  Outputs may not
+ * overlap inputs, each other or the workspace.
+ */
+adaln_status adaln_scale_residual_norm_bwd(const adaln_bf16 *d_out, const adaln_bf16 *d_r, const adaln_bf16 *x,
+                                           const adaln_bf16 *r, const adaln_bf16 *gate, const adaln_bf16 *emb,
+                                           const float *mean, const float *rstd, adaln_bf16 *d_x,
+                                           adaln_bf16 *d_residual, float *d_emb, float *d_gate, void *workspace,
+                                           size_t workspace_bytes, int B, int S, int D, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------ */
 

@@ -37,6 +37,10 @@ _SIGNATURES = {
     "adaln_proj_bwd_workspace_bytes": (_SZ, [_I, _I]),
     "adaln_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _I, _I, _P]),
     "adaln_proj_wgrad_rows": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "adaln_scale_residual_norm_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P]),
+    "adaln_scale_residual_norm_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "adaln_scale_residual_norm_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I,
+                                           _P]),
     "adaln_device_error": (_I, []),
 }
 
@@ -197,6 +201,56 @@ def adaln_out_bwd(dy, x, emb, mean, rstd, dx=None, d_emb=None, workspace=None, s
     _check("adaln_out_bwd", L.adaln_out_bwd(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd), _ptr(dx),
                                             _ptr(d_emb), _ptr(ws), nws, B, S, D, _stream(stream)))
     return dx, d_emb
+
+
+def adaln_scale_residual_norm_fwd(x, residual, gate, emb, r=None, out=None, mean=None, rstd=None, eps=1e-6,
+                                  stream=None):
+    """ScaleResidualLayerNormScaleShift forward: r = bf16(residual + bf16(gate
+    * x)), then the LayerNorm + modulation of r.  Returns (r, out, mean, rstd)."""
+    L = load()
+    B, S, D = x.shape
+    x = _input(x, torch.bfloat16, (B, S, D), "x")
+    residual = _input(residual, torch.bfloat16, (B, S, D), "residual")
+    gate = _input(gate, torch.bfloat16, (B, D), "gate")
+    emb = _input(emb, torch.bfloat16, (B, 2 * D), "emb")
+    r = _output(r, torch.bfloat16, (B, S, D), "r", x.device)
+    out = _output(out, torch.bfloat16, (B, S, D), "out", x.device)
+    mean = _output(mean, torch.float32, (B, S), "mean", x.device)
+    rstd = _output(rstd, torch.float32, (B, S), "rstd", x.device)
+    _check("adaln_scale_residual_norm_fwd",
+           L.adaln_scale_residual_norm_fwd(_ptr(x), _ptr(residual), _ptr(gate), _ptr(emb), _ptr(r), _ptr(out),
+                                           _ptr(mean), _ptr(rstd), B, S, D, float(eps), _stream(stream)))
+    return r, out, mean, rstd
+
+
+def adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D):
+    return load().adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D)
+
+
+def adaln_scale_residual_norm_bwd(d_out, d_r, x, r, gate, emb, mean, rstd, d_x=None, d_residual=None, d_emb=None,
+                                  d_gate=None, workspace=None, stream=None):
+    """Backward of adaln_scale_residual_norm_fwd; d_r (the gradient of r from
+    its later uses) may be None.  Returns (d_x, d_residual, d_emb, d_gate)."""
+    L = load()
+    B, S, D = x.shape
+    d_out = _input(d_out, torch.bfloat16, (B, S, D), "d_out")
+    d_r = None if d_r is None else _input(d_r, torch.bfloat16, (B, S, D), "d_r")
+    x = _input(x, torch.bfloat16, (B, S, D), "x")
+    r = _input(r, torch.bfloat16, (B, S, D), "r")
+    gate = _input(gate, torch.bfloat16, (B, D), "gate")
+    emb = _input(emb, torch.bfloat16, (B, 2 * D), "emb")
+    mean = _input(mean, torch.float32, (B, S), "mean")
+    rstd = _input(rstd, torch.float32, (B, S), "rstd")
+    d_x = _output(d_x, torch.bfloat16, (B, S, D), "d_x", x.device)
+    d_residual = _output(d_residual, torch.bfloat16, (B, S, D), "d_residual", x.device)
+    d_emb = _output(d_emb, torch.float32, (B, 2 * D), "d_emb", x.device)
+    d_gate = _output(d_gate, torch.float32, (B, D), "d_gate", x.device)
+    ws, nws = _workspace(workspace, L.adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D), x.device)
+    _check("adaln_scale_residual_norm_bwd",
+           L.adaln_scale_residual_norm_bwd(_ptr(d_out), _ptr(d_r), _ptr(x), _ptr(r), _ptr(gate), _ptr(emb),
+                                           _ptr(mean), _ptr(rstd), _ptr(d_x), _ptr(d_residual), _ptr(d_emb),
+                                           _ptr(d_gate), _ptr(ws), nws, B, S, D, _stream(stream)))
+    return d_x, d_residual, d_emb, d_gate
 
 
 def adaln_out_bwd_noalloc(dy, x, emb, mean, rstd, dx=None, d_emb=None, stream=None):

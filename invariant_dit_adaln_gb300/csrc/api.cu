@@ -249,6 +249,62 @@ adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H, vo
     return from_cuda(launch_token_tree(in, out, workspace, B, S, H, (cudaStream_t)stream, dev));
 }
 
+size_t adaln_scale_residual_norm_bwd_workspace_bytes(int B, int S, int D) {
+    // the LayerNorm backward's tree nodes (2D columns), then the gate's (D
+    // columns) in the same space
+    return adaln_out_bwd_workspace_bytes(B, S, D);
+}
+
+adaln_status adaln_scale_residual_norm_fwd(const adaln_bf16 *x, const adaln_bf16 *residual, const adaln_bf16 *gate,
+                                           const adaln_bf16 *emb, adaln_bf16 *r, adaln_bf16 *out, float *mean,
+                                           float *rstd, int B, int S, int D, float eps, void *stream) {
+    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return ADALN_ERR_ARG;
+    const size_t rows = (size_t)B * S;
+    const Buf ins[] = {{x, rows * D * 2}, {residual, rows * D * 2}, {gate, (size_t)B * D * 2},
+                       {emb, (size_t)B * 2 * D * 2}};
+    const Buf outs[] = {{r, rows * D * 2}, {out, rows * D * 2}, {mean, rows * 4}, {rstd, rows * 4}};
+    if (any_missing(ins, 4) || any_missing(outs, 4)) return ADALN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(gate) || !aligned16(emb) || !aligned16(r) ||
+        !aligned16(out) || !aligned16(mean) || !aligned16(rstd))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 4, ins, 4)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (rows == 0) return ADALN_OK;
+    return from_cuda(launch_res_fwd(x, residual, gate, emb, r, out, mean, rstd, B, S, D, eps, (cudaStream_t)stream,
+                                    dev));
+}
+
+adaln_status adaln_scale_residual_norm_bwd(const adaln_bf16 *d_out, const adaln_bf16 *d_r, const adaln_bf16 *x,
+                                           const adaln_bf16 *r, const adaln_bf16 *gate, const adaln_bf16 *emb,
+                                           const float *mean, const float *rstd, adaln_bf16 *d_x,
+                                           adaln_bf16 *d_residual, float *d_emb, float *d_gate, void *workspace,
+                                           size_t workspace_bytes, int B, int S, int D, void *stream) {
+    if (!valid_D(D) || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    const size_t rows = (size_t)B * S;
+    const size_t need = adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D);
+    const Buf ins[] = {{d_out, rows * D * 2}, {x, rows * D * 2}, {r, rows * D * 2}, {gate, (size_t)B * D * 2},
+                       {emb, (size_t)B * 2 * D * 2}, {mean, rows * 4}, {rstd, rows * 4},
+                       {d_r, d_r ? rows * D * 2 : 0}};
+    const Buf outs[] = {{d_x, rows * D * 2}, {d_residual, rows * D * 2}, {d_emb, (size_t)B * 2 * D * 4},
+                        {d_gate, (size_t)B * D * 4}, {workspace, need}};
+    if (any_missing(ins, 7) || any_missing(outs, 4)) return ADALN_ERR_NULL;
+    if (!aligned16(d_out) || !aligned16(d_r) || !aligned16(x) || !aligned16(r) || !aligned16(gate) ||
+        !aligned16(emb) || !aligned16(mean) || !aligned16(rstd) || !aligned16(d_x) || !aligned16(d_residual) ||
+        !aligned16(d_emb) || !aligned16(d_gate) || !aligned16(workspace))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 5, ins, 8)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_res_bwd(d_out, d_r, x, r, gate, emb, mean, rstd, d_x, d_residual, d_emb, d_gate,
+                                    workspace, B, S, D, (cudaStream_t)stream, dev));
+}
+
 adaln_status adaln_proj_bwd(const float *d_emb, const adaln_bf16 *temb, const adaln_bf16 *u, const adaln_bf16 *W,
                             adaln_bf16 *d_temb, float *dW_acc, float *db_acc, adaln_bf16 *dW, adaln_bf16 *db,
                             int accumulate, void *workspace, size_t workspace_bytes, int B, int D, void *stream) {

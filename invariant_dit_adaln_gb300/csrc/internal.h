@@ -62,6 +62,19 @@ cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t
 cudaError_t launch_token_tree(const float *in, float *out, void *ws, int B, int S, int H, cudaStream_t stream,
                               const DeviceInfo &dev);
 int read_and_clear_device_error();
+// the token tree's levels >= 1 from level-0 nodes sig, kap [B][T][H]; zero fill
+cudaError_t launch_fold(const float *sig, const float *kap, float *out, int B, int T, int H, cudaStream_t stream,
+                        const DeviceInfo &dev);
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream);
+
+// res.cu: the block-level modulated norm with a gated residual
+cudaError_t launch_res_fwd(const uint16_t *x, const uint16_t *residual, const uint16_t *gate, const uint16_t *emb,
+                           uint16_t *r, uint16_t *out, float *mean, float *rstd, int B, int S, int D, float eps,
+                           cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_res_bwd(const uint16_t *d_out, const uint16_t *d_r, const uint16_t *x, const uint16_t *r,
+                           const uint16_t *gate, const uint16_t *emb, const float *mean, const float *rstd,
+                           uint16_t *d_x, uint16_t *d_residual, float *d_emb, float *d_gate, void *ws, int B, int S,
+                           int D, cudaStream_t stream, const DeviceInfo &dev);
 
 // proj.cu
 cudaError_t launch_proj_fwd(const uint16_t *temb, const uint16_t *W, const uint16_t *bias, uint16_t *emb,

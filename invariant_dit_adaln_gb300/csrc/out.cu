@@ -1043,8 +1043,8 @@ __global__ void zero_kernel(float *__restrict__ p, size_t n) {
 // --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
-static cudaError_t launch_fold(const float *sig, const float *kap, float *out, int B, int T, int H,
-                               cudaStream_t stream, const DeviceInfo &dev) {
+cudaError_t launch_fold(const float *sig, const float *kap, float *out, int B, int T, int H, cudaStream_t stream,
+                        const DeviceInfo &dev) {
     const int n1 = (T + kTile - 1) / kTile;
     const int warps = T == 1 ? 1 : min(kFoldWarps, n1);
     const size_t smem = fold_smem_bytes(n1);
@@ -1054,7 +1054,7 @@ static cudaError_t launch_fold(const float *sig, const float *kap, float *out, i
                       sig, kap, out, T, H);
 }
 
-static cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream) {
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
     return launch_pdl(zero_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, p, n);
 }

@@ -41,7 +41,7 @@ def fake(i, off=0):
 
 def test_library_exports_every_declared_symbol(L):
     names = binding.declared_symbols()
-    assert len(names) == 13, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(L, n), n
     assert L.adaln_version() >> 16 == 1
@@ -213,6 +213,45 @@ def test_proj_wgrad_rows_checks(L, no_gpu):
     assert wgrad_rows(L, dW=fake(4, 8)) == ALIGN
     assert wgrad_rows(L, dW=fake(0, 64)) == ALIAS            # dW inside d_emb
     assert wgrad_rows(L) == DEVICE                          # valid: the device check comes next
+
+
+# --- adaln_scale_residual_norm_fwd / _bwd ------------------------------------
+
+def res_fwd(L, x=0, residual=1, gate=2, emb=3, r=4, out=5, mean=6, rstd=7, B=2, S=33, D=3072, eps=1e-6):
+    p = [None if a is None else (fake(a) if isinstance(a, int) else a)
+         for a in (x, residual, gate, emb, r, out, mean, rstd)]
+    return L.adaln_scale_residual_norm_fwd(*p, B, S, D, ctypes.c_float(eps), None)
+
+
+def res_bwd(L, d_out=0, d_r=1, x=2, r=3, gate=4, emb=5, mean=6, rstd=7, d_x=8, d_res=9, d_emb=10, d_gate=11,
+            ws=12, nws=None, B=2, S=33, D=3072):
+    p = [None if a is None else (fake(a) if isinstance(a, int) else a)
+         for a in (d_out, d_r, x, r, gate, emb, mean, rstd, d_x, d_res, d_emb, d_gate)]
+    wsp = None if ws is None else (fake(ws) if isinstance(ws, int) else ws)
+    if nws is None:
+        nws = L.adaln_scale_residual_norm_bwd_workspace_bytes(B, S, D)
+    return L.adaln_scale_residual_norm_bwd(*p, wsp, nws, B, S, D, None)
+
+
+def test_scale_residual_norm_checks(L, no_gpu):
+    assert L.adaln_scale_residual_norm_bwd_workspace_bytes(2, 33, 3072) == L.adaln_out_bwd_workspace_bytes(2, 33, 3072)
+    assert res_fwd(L, D=12) == SHAPE
+    assert res_fwd(L, eps=-1.0) == ARG
+    assert res_fwd(L, gate=None) == NULL
+    assert res_fwd(L, r=None) == NULL
+    assert res_fwd(L, r=fake(4, 8)) == ALIGN
+    assert res_fwd(L, r=fake(1, 64)) == ALIAS             # r inside residual (no in-place form)
+    assert res_fwd(L, out=fake(4, 1024)) == ALIAS         # out overlaps r
+    assert res_fwd(L) == DEVICE
+    assert res_bwd(L, S=-1) == SHAPE
+    assert res_bwd(L, x=None) == NULL
+    assert res_bwd(L, d_gate=None) == NULL
+    assert res_bwd(L, d_r=None) == DEVICE                 # d_r is optional
+    assert res_bwd(L, d_x=fake(8, 2)) == ALIGN
+    assert res_bwd(L, d_res=fake(1, 0)) == ALIAS          # d_residual is d_r
+    assert res_bwd(L, d_gate=fake(12, 0)) == ALIAS        # d_gate inside the workspace
+    assert res_bwd(L, nws=16) == WORKSPACE
+    assert res_bwd(L) == DEVICE
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="a valid call with fake pointers would launch on a GPU")
