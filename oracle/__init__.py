@@ -69,6 +69,12 @@ def _load():
             "oracle_res_bwd_tail": [P, P, P, P, P, P, P, I, I, I],
             "oracle_res_bwd": [P, P, P, P, P, P, F, P, P, P, P, I, I, I],
             "oracle_res_gate_products_f32": [P, P, P, Lg],
+            "oracle_f32_proj_fwd": [P, P, P, P, P, I, I],
+            "oracle_f32_out_fwd": [P, P, F, P, P, P, I, I, I],
+            "oracle_f32_out_bwd": [P, P, P, F, P, P, I, I, I],
+            "oracle_f32_bwd_products": [P, P, P, P, P, I, I, I],
+            "oracle_f32_proj_bwd": [P, P, P, P, P, P, I, I],
+            "oracle_f32_wgrad_seq": [P, P, P, P, I, I, I],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -319,6 +325,68 @@ def res_gate_products_f32(gr, x):
     prod = np.empty(x.shape, dtype=np.float32)
     _load().oracle_res_gate_products_f32(_p(gr), _p(x), _p(prod), x.size)
     return prod
+
+
+# --- fp32 execution dtype ----------------------------------------------------
+
+def _f(a):
+    return _c(a, np.float32)
+
+
+def f32_proj_fwd(temb, W, b):
+    """(emb [B,2D] fp32, u [B,D] fp32) of the fp32 operator."""
+    temb, W, b = _f(temb), _f(W), _f(b)
+    B, D = temb.shape
+    emb = np.empty((B, 2 * D), np.float32)
+    u = np.empty((B, D), np.float32)
+    _load().oracle_f32_proj_fwd(_p(temb), _p(W), _p(b), _p(emb), _p(u), B, D)
+    return emb, u
+
+
+def f32_out_fwd(x, emb, eps=EPS):
+    x, emb = _f(x), _f(emb)
+    B, S, D = x.shape
+    out = np.empty_like(x)
+    mean = np.empty((B, S), np.float32)
+    rstd = np.empty((B, S), np.float32)
+    _load().oracle_f32_out_fwd(_p(x), _p(emb), float(eps), _p(out), _p(mean), _p(rstd), B, S, D)
+    return out, mean, rstd
+
+
+def f32_out_bwd(dy, x, emb, eps=EPS):
+    dy, x, emb = _f(dy), _f(x), _f(emb)
+    B, S, D = x.shape
+    dx = np.empty_like(x)
+    d_emb = np.empty((B, 2 * D), np.float32)
+    _load().oracle_f32_out_bwd(_p(dy), _p(x), _p(emb), float(eps), _p(dx), _p(d_emb), B, S, D)
+    return dx, d_emb
+
+
+def f32_bwd_products(dy, x, mean, rstd):
+    dy, x, mean, rstd = _f(dy), _f(x), _f(mean), _f(rstd)
+    B, S, D = x.shape
+    prod = np.empty((B, S, 2 * D), np.float32)
+    _load().oracle_f32_bwd_products(_p(dy), _p(x), _p(mean), _p(rstd), _p(prod), B, S, D)
+    return prod
+
+
+def f32_proj_bwd(d_emb, temb, W, want_dW=True):
+    d_emb, temb, W = _f(d_emb), _f(temb), _f(W)
+    B, D = temb.shape
+    d_temb = np.empty((B, D), np.float32)
+    dW = np.empty((2 * D, D), np.float32) if want_dW else None
+    db = np.empty(2 * D, np.float32) if want_dW else None
+    _load().oracle_f32_proj_bwd(_p(d_emb), _p(temb), _p(W), _p(d_temb), _p(dW), _p(db), B, D)
+    return d_temb, dW, db
+
+
+def f32_wgrad_seq(d_emb, u, dW_acc=None, db_acc=None, accumulate=False):
+    d_emb, u = _f(d_emb), _f(u)
+    B, D = u.shape
+    dW = np.zeros((2 * D, D), np.float32) if dW_acc is None else _f(dW_acc).copy()
+    db = np.zeros(2 * D, np.float32) if db_acc is None else _f(db_acc).copy()
+    _load().oracle_f32_wgrad_seq(_p(d_emb), _p(u), _p(dW), _p(db), int(bool(accumulate)), B, D)
+    return dW, db
 
 
 def bf16_from_f64(a):

@@ -657,6 +657,171 @@ void oracle_res_gate_products_f32(const uint16_t *gr, const uint16_t *x, float *
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP32 execution dtype (RL-Kernel PR 538 "Results": the FP32 timings and the */
+/* BF16/FP32 acceptance gates): the same operator on fp32 tensors with no    */
+/* bf16 rounding anywhere; every eager fp32 operation rounds once to fp32.   */
+/* ------------------------------------------------------------------------ */
+
+/* u = fp32(silu(t)) (the fp32 nearest to the fp64 value);
+ * emb[b,n] = fp32(sum_k u[b,k] W[n,k] + bias[n]), the sum exact (compensated
+ * fp64 over the fp64-exact products of two fp32 values), rounded once.       */
+void oracle_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B, int D)
+{
+    int N = 2 * D;
+    double *ud = malloc(sizeof(double) * (size_t)B * D);
+    double *wd = malloc(sizeof(double) * (size_t)N * D);
+    double *bd = malloc(sizeof(double) * (size_t)N);
+    double *e = malloc(sizeof(double) * (size_t)B * N);
+    for (size_t i = 0; i < (size_t)B * D; ++i) {
+        u[i] = (float)silu64((double)temb[i]);
+        ud[i] = (double)u[i];
+    }
+    for (size_t i = 0; i < (size_t)N * D; ++i) wd[i] = (double)W[i];
+    for (int n = 0; n < N; ++n) bd[n] = (double)bias[n];
+    proj_core(ud, wd, bd, e, B, D, N, 0, N);
+    for (size_t i = 0; i < (size_t)B * N; ++i) emb[i] = (float)e[i];
+    free(ud); free(wd); free(bd); free(e);
+}
+
+/* xhat = fp32(exact LayerNorm of x); onep = fp32(1 + scale);
+ * out = fp32(fp32(xhat * onep) + shift); mean, rstd = fp32 of the exact
+ * row statistics (nullable).                                                 */
+void oracle_f32_out_fwd(const float *x, const float *emb, float eps, float *out, float *mean, float *rstd, int B,
+                        int S, int D)
+{
+    double *xr = malloc(sizeof(double) * (size_t)D);
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        const float *sc = emb + (size_t)b * 2 * D, *sh = sc + D;
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            for (int d = 0; d < D; ++d) xr[d] = (double)x[row * D + d];
+            double mu, r;
+            ln_row(xr, D, (double)eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d) {
+                float onep = 1.0f + sc[d];
+                float prod = (float)xh[d] * onep;
+                out[row * D + d] = prod + sh[d];
+            }
+            if (mean) mean[row] = (float)mu;
+            if (rstd) rstd[row] = (float)r;
+        }
+    }
+    free(xr); free(xh);
+}
+
+/* dx = fp32(exact LayerNorm backward of g * onep), g = dy, onep = fp32(1 +
+ * scale); d_emb[b, 0:D] = sum_s g * fp32(xhat), d_emb[b, D:2D] = sum_s g,
+ * exact sums rounded once to fp32.                                           */
+void oracle_f32_out_bwd(const float *dy, const float *x, const float *emb, float eps, float *dx, float *d_emb,
+                        int B, int S, int D)
+{
+    double *xr = malloc(sizeof(double) * (size_t)D);
+    double *xh = malloc(sizeof(double) * (size_t)D);
+    double *gh = malloc(sizeof(double) * (size_t)D);
+    double *dxr = malloc(sizeof(double) * (size_t)D);
+    nsum *ss = malloc(sizeof(nsum) * (size_t)D);
+    nsum *sh = malloc(sizeof(nsum) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        const float *sc = emb + (size_t)b * 2 * D;
+        for (int d = 0; d < D; ++d) ss[d].s = ss[d].c = sh[d].s = sh[d].c = 0.0;
+        for (int s = 0; s < S; ++s) {
+            size_t row = (size_t)b * S + s;
+            for (int d = 0; d < D; ++d) xr[d] = (double)x[row * D + d];
+            double mu, r;
+            ln_row(xr, D, (double)eps, &mu, &r, xh);
+            for (int d = 0; d < D; ++d) {
+                double g = (double)dy[row * D + d];
+                gh[d] = g * (double)(1.0f + sc[d]);          /* exact */
+                nsum_add(&ss[d], g * (double)(float)xh[d]);  /* exact */
+                nsum_add(&sh[d], g);
+            }
+            ln_bwd_row(gh, xh, r, D, dxr);
+            for (int d = 0; d < D; ++d) dx[row * D + d] = (float)dxr[d];
+        }
+        for (int d = 0; d < D; ++d) {
+            d_emb[(size_t)b * 2 * D + d] = (float)nsum_val(&ss[d]);
+            d_emb[(size_t)b * 2 * D + D + d] = (float)nsum_val(&sh[d]);
+        }
+    }
+    free(xr); free(xh); free(gh); free(dxr); free(ss); free(sh);
+}
+
+/* the fp32 backward's token products from saved statistics:
+ * xhat = fp32(fp32(x - mean) * rstd); prod = (fp32(g * xhat), g)             */
+void oracle_f32_bwd_products(const float *dy, const float *x, const float *mean, const float *rstd, float *prod,
+                             int B, int S, int D)
+{
+    for (size_t row = 0; row < (size_t)B * S; ++row)
+        for (int d = 0; d < D; ++d) {
+            float xc = x[row * D + d] - mean[row];
+            float xh = xc * rstd[row];
+            float g = dy[row * D + d];
+            prod[row * 2 * D + d] = g * xh;
+            prod[row * 2 * D + D + d] = g;
+        }
+}
+
+/* d_temb = fp32(sum_n e W * silu'(t)) with e = d_emb (no rounding), u =
+ * fp32(silu(t)); dW = fp32(sum_b e u), db = fp32(sum_b e): exact sums,
+ * rounded once (d_temb's product with silu'(t) exact in fp64 too).           */
+void oracle_f32_proj_bwd(const float *d_emb, const float *temb, const float *W, float *d_temb, float *dW,
+                         float *db, int B, int D)
+{
+    int N = 2 * D;
+    nsum *acc = malloc(sizeof(nsum) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        for (int k = 0; k < D; ++k) acc[k].s = acc[k].c = 0.0;
+        for (int n = 0; n < N; ++n) {
+            double e = (double)d_emb[(size_t)b * N + n];
+            const float *w = W + (size_t)n * D;
+            for (int k = 0; k < D; ++k) nsum_add(&acc[k], e * (double)w[k]);
+        }
+        for (int k = 0; k < D; ++k) {
+            double t = (double)temb[(size_t)b * D + k];
+            d_temb[(size_t)b * D + k] = (float)(nsum_val(&acc[k]) * dsilu64(t));
+        }
+    }
+    free(acc);
+    if (dW || db) {
+        double *u = malloc(sizeof(double) * (size_t)B * D);
+        for (size_t i = 0; i < (size_t)B * D; ++i) u[i] = (double)(float)silu64((double)temb[i]);
+        for (int n = 0; n < N; ++n) {
+            nsum a = {0.0, 0.0};
+            if (dW)
+                for (int k = 0; k < D; ++k) {
+                    nsum w = {0.0, 0.0};
+                    for (int b = 0; b < B; ++b) nsum_add(&w, (double)d_emb[(size_t)b * N + n] * u[(size_t)b * D + k]);
+                    dW[(size_t)n * D + k] = (float)nsum_val(&w);
+                }
+            for (int b = 0; b < B; ++b) nsum_add(&a, (double)d_emb[(size_t)b * N + n]);
+            if (db) db[n] = (float)nsum_val(&a);
+        }
+        free(u);
+    }
+}
+
+/* The fp32 weight gradient in the operator's fixed order: from the caller's
+ * accumulators (accumulate != 0) or +0, samples in ascending order, one fused
+ * multiply-add per sample, acc = fma(e[b,n], u[b,k], acc) (one rounding);
+ * db_acc[n] = db_acc[n] + e[b,n].  u as given (the forward's fp32 u).        */
+void oracle_f32_wgrad_seq(const float *d_emb, const float *u, float *dW_acc, float *db_acc, int accumulate, int B,
+                          int D)
+{
+    int N = 2 * D;
+    for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < D; ++k) {
+            float a = accumulate ? dW_acc[(size_t)n * D + k] : 0.0f;
+            for (int b = 0; b < B; ++b) a = fmaf(d_emb[(size_t)b * N + n], u[(size_t)b * D + k], a);
+            dW_acc[(size_t)n * D + k] = a;
+        }
+        float a = accumulate ? db_acc[n] : 0.0f;
+        for (int b = 0; b < B; ++b) a = a + d_emb[(size_t)b * N + n];
+        db_acc[n] = a;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* format helpers exported for the tests                                     */
 /* ------------------------------------------------------------------------ */
 

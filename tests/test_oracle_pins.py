@@ -730,3 +730,154 @@ def test_res_bwd_is_the_norm_backward_then_the_tail(orc):
     bound = 2.0 ** -23 * np.abs(exact) + 2.0 ** -30 * np.abs(prod).astype(np.float64).sum(axis=1)
     assert np.all(np.abs(tree - exact) <= bound + 2.0 ** -24 * np.abs(exact))
     assert np.all(np.abs(d_gate.astype(np.float64) - exact) <= 2.0 ** -24 * np.abs(exact))
+
+
+# ---------------------------------------------------------------------------
+# fp32 execution dtype (RL-Kernel PR 538 "Results": the FP32 timings and gates)
+# ---------------------------------------------------------------------------
+
+def _f32_inputs(B, S, D, seed):
+    rng = np.random.default_rng(seed)
+    return {"x": rng.standard_normal((B, S, D)).astype(np.float32),
+            "dy": rng.standard_normal((B, S, D)).astype(np.float32),
+            "temb": rng.standard_normal((B, D)).astype(np.float32),
+            "W": (rng.standard_normal((2 * D, D)) * 0.02).astype(np.float32),
+            "b": (rng.standard_normal(2 * D) * 0.02).astype(np.float32)}
+
+
+def _ulp32(a, b):
+    ia = np.asarray(a, np.float32).view(np.int32).astype(np.int64)
+    ib = np.asarray(b, np.float32).view(np.int32).astype(np.int64)
+    ia = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
+    ib = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
+    return np.abs(ia - ib)
+
+
+def test_f32_proj_fwd_exact(orc):
+    """u = the fp32 nearest to silu(t) (mpmath at 200 bits); emb = the exact
+    rational sum of u W + bias rounded once to fp32, bit for bit."""
+    import mpmath
+    mpmath.mp.prec = 200
+    B, D = 2, 8
+    i = _f32_inputs(B, 1, D, 40)
+    emb, u = orc.f32_proj_fwd(i["temb"], i["W"], i["b"])
+    for b in range(B):
+        for k in range(D):
+            t = mpmath.mpf(float(i["temb"][b, k]))
+            s = t / (1 + mpmath.exp(-t))
+            mag = Fraction(int(s.man)) * Fraction(2) ** int(s.exp)
+            assert Fraction(float(u[b, k])) == f32_exact_round(-mag if s < 0 else mag), (b, k)
+    for b in range(B):
+        for n in range(2 * D):
+            v = sum(Fraction(float(u[b, k])) * Fraction(float(i["W"][n, k])) for k in range(D))
+            v += Fraction(float(i["b"][n]))
+            assert Fraction(float(emb[b, n])) == f32_exact_round(v), (b, n)
+
+
+def test_f32_out_fwd_rounding_points(orc):
+    """out = fp32(fp32(xhat * fp32(1 + scale)) + shift) with xhat the fp32 of
+    numpy's fp64 LayerNorm; the fused form and an unrounded (1 + scale) each
+    give different bits somewhere, so neither could pass."""
+    B, S, D = 2, 6, 64
+    i = _f32_inputs(B, S, D, 41)
+    emb = (np.random.default_rng(42).standard_normal((B, 2 * D)) * 0.3).astype(np.float32)
+    out, mean, rstd = orc.f32_out_fwd(i["x"], emb)
+    x = i["x"].astype(np.float64)
+    mu = x.mean(-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(-1, keepdims=True)
+    r = 1.0 / np.sqrt(var + EPS32)
+    xh = ((x - mu) * r).astype(np.float32)
+    onep = (np.float32(1) + emb[:, None, :D]).astype(np.float32)
+    shift = emb[:, None, D:]
+    want = (xh * onep).astype(np.float32) + shift
+    assert np.all(_ulp32(out, want) <= 1) and (out == want).mean() > 0.999
+    assert np.all(_ulp32(mean, mu[..., 0].astype(np.float32)) <= 1)
+    assert np.all(_ulp32(rstd, r[..., 0].astype(np.float32)) <= 1)
+    fused = (xh.astype(np.float64) * onep + shift).astype(np.float32)
+    raw_onep = ((xh.astype(np.float64) * (1.0 + emb[:, None, :D].astype(np.float64))).astype(np.float32) + shift)
+    assert np.any(fused != out) and np.any(raw_onep != out)
+
+
+def test_f32_out_bwd_matches_torch_autograd(orc):
+    """dx: torch fp64 autograd of xhat * onep (onep = fp32(1 + scale)) rounded
+    to fp32, within 1 ulp; d_scale, d_shift: math.fsum of g * fp32(xhat) and of
+    g, rounded once, bit for bit."""
+    B, S, D = 2, 7, 48
+    i = _f32_inputs(B, S, D, 43)
+    emb = (np.random.default_rng(44).standard_normal((B, 2 * D)) * 0.3).astype(np.float32)
+    dx, d_emb = orc.f32_out_bwd(i["dy"], i["x"], emb)
+    x = torch.tensor(i["x"], dtype=torch.float64, requires_grad=True)
+    onep = torch.tensor((np.float32(1) + emb[:, :D]).astype(np.float64))[:, None, :]
+    y = torch.nn.functional.layer_norm(x, (D,), eps=EPS32) * onep
+    y.backward(torch.tensor(i["dy"], dtype=torch.float64))
+    want = x.grad.numpy().astype(np.float32)
+    assert np.all(_ulp32(dx, want) <= 1) and (dx == want).mean() > 0.99
+    xd = i["x"].astype(np.float64)
+    mu = xd.mean(-1, keepdims=True)
+    xh = ((xd - mu) / np.sqrt(((xd - mu) ** 2).mean(-1, keepdims=True) + EPS32)).astype(np.float32)
+    g = i["dy"].astype(np.float64)
+    for b in range(B):
+        for d in range(D):
+            assert d_emb[b, d] == np.float32(math.fsum(g[b, :, d] * xh[b, :, d].astype(np.float64)))
+            assert d_emb[b, D + d] == np.float32(math.fsum(g[b, :, d]))
+
+
+def test_f32_bwd_products_are_numpy_fp32_ops(orc):
+    B, S, D = 2, 5, 32
+    i = _f32_inputs(B, S, D, 45)
+    rng = np.random.default_rng(46)
+    mean = (rng.standard_normal((B, S)) * 2).astype(np.float32)
+    rstd = np.exp(rng.uniform(-3, 3, (B, S))).astype(np.float32)
+    prod = orc.f32_bwd_products(i["dy"], i["x"], mean, rstd)
+    xh = ((i["x"] - mean[..., None]).astype(np.float32) * rstd[..., None]).astype(np.float32)
+    assert_bitwise(prod[..., :D], (i["dy"] * xh).astype(np.float32), "g * xhat")
+    assert_bitwise(prod[..., D:], i["dy"], "g")
+
+
+def test_f32_proj_bwd_matches_torch_autograd(orc):
+    """d_temb, dW, db: torch fp64 autograd of emb = fp32(silu(t)) @ W^T + b
+    (the fp32 u treated as exact, silu' of t analytic), rounded to fp32."""
+    B, D = 3, 16
+    i = _f32_inputs(B, 1, D, 47)
+    d_emb = np.random.default_rng(48).standard_normal((B, 2 * D)).astype(np.float32)
+    d_temb, dW, db = orc.f32_proj_bwd(d_emb, i["temb"], i["W"])
+    t = torch.tensor(i["temb"], dtype=torch.float64, requires_grad=True)
+    s = torch.sigmoid(t)
+    u32 = torch.tensor(orc.f32_proj_fwd(i["temb"], i["W"], i["b"])[1], dtype=torch.float64)
+    u = u32 + (t * s - (t * s).detach())  # value fp32(silu(t)), gradient silu'(t)
+    W = torch.tensor(i["W"], dtype=torch.float64, requires_grad=True)
+    bb = torch.tensor(i["b"], dtype=torch.float64, requires_grad=True)
+    (u @ W.T + bb).backward(torch.tensor(d_emb, dtype=torch.float64))
+    assert np.all(_ulp32(d_temb, t.grad.numpy().astype(np.float32)) <= 1)
+    assert np.all(_ulp32(dW, W.grad.numpy().astype(np.float32)) <= 1)
+    assert np.all(_ulp32(db, bb.grad.numpy().astype(np.float32)) <= 1)
+
+
+def test_f32_wgrad_seq_is_a_sequential_fused_multiply_add(orc):
+    """acc = fp32(e * u + acc) (one rounding) over samples in ascending order,
+    against exact rationals; a separately rounded product would differ."""
+    B, D = 5, 6
+    rng = np.random.default_rng(49)
+    e = rng.standard_normal((B, 2 * D)).astype(np.float32)
+    u = rng.standard_normal((B, D)).astype(np.float32)
+    dW, db = orc.f32_wgrad_seq(e, u)
+    unfused = 0
+    for n in range(2 * D):
+        for k in range(D):
+            a = Fraction(0)
+            a2 = np.float32(0)
+            for b in range(B):
+                a = f32_exact_round(Fraction(float(e[b, n])) * Fraction(float(u[b, k])) + a)
+                a2 = np.float32(a2 + np.float32(e[b, n] * u[b, k]))
+            assert Fraction(float(dW[n, k])) == a, (n, k)
+            unfused += float(a2) != float(a)
+    assert unfused > 0
+    db_want = np.zeros(2 * D, np.float32)
+    for b in range(B):
+        db_want = (db_want + e[b]).astype(np.float32)
+    assert_bitwise(db, db_want, "db")
+    # accumulate: continuing from the accumulators equals one longer sequence
+    dW1, db1 = orc.f32_wgrad_seq(e[:2], u[:2])
+    dW2, db2 = orc.f32_wgrad_seq(e[2:], u[2:], dW1, db1, accumulate=True)
+    assert_bitwise(dW2, dW, "chunked dW")
+    assert_bitwise(db2, db, "chunked db")
