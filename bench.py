@@ -974,10 +974,11 @@ def run_block(args, rank, local):
     passes = []
     for _ in range(5):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            graphs[i % 2].replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream: the events' stream
+            e0.record(stream)
+            for i in range(K):
+                graphs[i % 2].replay()
+            e1.record(stream)
         torch.cuda.synchronize()
         passes.append(e0.elapsed_time(e1) / K)
     if binding.device_error() != 0:
@@ -992,6 +993,91 @@ def run_block(args, rank, local):
                       "kernels_per_step": 6, "steps_per_pass": K, "passes": len(passes),
                       "l2": "two input sets alternate (each: four 50.3 MB token inputs and four 50.3 MB token outputs, more than L2); no flush",
                       "data": "synthetic (seeded, drawn on the device)"}), flush=True)
+
+
+def run_f32(args, rank, local):
+    """The fp32 execution dtype: the whole step (adaln_f32_proj_fwd,
+    adaln_f32_out_fwd, adaln_f32_out_bwd, adaln_f32_proj_bwd with dW, db) at
+    B=2, S=4096, D=3072: K steps replayed from CUDA graphs over two input sets
+    larger than L2, median of passes; one JSON line on rank 0 with tokens/s
+    and the algorithmic HBM bytes against the measured copy peak."""
+    if rank != 0:
+        return
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    build.build()
+    binding.load()
+    B, S, D = 2, 4096, 3072
+    N = 2 * D
+    g = torch.Generator(device="cuda")
+    g.manual_seed(WORKLOAD["seed"])
+    W = torch.randn((N, D), generator=g, device="cuda") * 0.02
+    bias = torch.randn((N,), generator=g, device="cuda") * 0.02
+
+    def make():
+        t = {"x": torch.randn((B, S, D), generator=g, device="cuda"),
+             "dy": torch.randn((B, S, D), generator=g, device="cuda"),
+             "temb": torch.randn((B, D), generator=g, device="cuda")}
+        t["emb"], t["u"] = torch.empty((B, N), device="cuda"), torch.empty((B, D), device="cuda")
+        t["out"], t["dx"] = torch.empty((B, S, D), device="cuda"), torch.empty((B, S, D), device="cuda")
+        t["mean"], t["rstd"] = torch.empty((B, S), device="cuda"), torch.empty((B, S), device="cuda")
+        t["d_emb"], t["d_temb"] = torch.empty((B, N), device="cuda"), torch.empty((B, D), device="cuda")
+        t["dW"], t["db"] = torch.empty((N, D), device="cuda"), torch.empty((N,), device="cuda")
+        t["ws1"] = torch.empty(binding.adaln_f32_out_bwd_workspace_bytes(B, S, D), dtype=torch.uint8, device="cuda")
+        t["ws2"] = torch.empty(binding.adaln_f32_proj_bwd_workspace_bytes(B, D), dtype=torch.uint8, device="cuda")
+        return t
+
+    sets = [make(), make()]
+    stream = torch.cuda.Stream()
+
+    def step(t):
+        binding.adaln_f32_proj_fwd(t["temb"], W, bias, emb=t["emb"], u=t["u"], stream=stream)
+        binding.adaln_f32_out_fwd(t["x"], t["emb"], out=t["out"], mean=t["mean"], rstd=t["rstd"], stream=stream)
+        binding.adaln_f32_out_bwd(t["dy"], t["x"], t["emb"], t["mean"], t["rstd"], dx=t["dx"], d_emb=t["d_emb"],
+                                  workspace=t["ws1"], stream=stream)
+        binding.adaln_f32_proj_bwd(t["d_emb"], t["temb"], t["u"], W, d_temb=t["d_temb"], dW_acc=t["dW"],
+                                   db_acc=t["db"], workspace=t["ws2"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for t in sets:
+                step(t)
+    torch.cuda.synchronize()
+    graphs = []
+    for t in sets:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(t)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+    K = min(args.steps, 1000)
+    passes = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream: the events' stream
+            e0.record(stream)
+            for i in range(K):
+                graphs[i % 2].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        passes.append(e0.elapsed_time(e1) / K)
+    if binding.device_error() != 0:
+        raise RuntimeError("device-side error in the fp32 workload")
+    ms = statistics.median(passes)
+    tok, wb = B * S * D * 4, N * D * 4
+    alg = (wb + N * 4 + 2 * B * D * 4 + B * N * 4          # projection forward
+           + 2 * tok + B * S * 8 + B * N * 4                # LayerNorm forward
+           + 3 * tok + B * S * 8 + 2 * B * N * 4            # LayerNorm backward
+           + 2 * wb + N * 4 + B * N * 4 + 3 * B * D * 4)    # projection backward (dW, db written)
+    peak, peak_src = hbm_peak()
+    print(json.dumps({"workload": "fp32 execution dtype, fwd+bwd, B=2 S=4096 D=3072", "value": B * S / (ms / 1e3),
+                      "unit": "tokens/s", "ms_per_step": ms, "algorithmic_bytes_per_step": alg,
+                      "hbm_gbs": alg / (ms / 1e3) / 1e9, "hbm_frac": alg / (ms / 1e3) / 1e9 / peak, "peak_gbs": peak,
+                      "peak_source": peak_src, "kernels_per_step": 7, "steps_per_pass": K, "passes": len(passes),
+                      "l2": "two input sets alternate (x, dy 100.7 MB each per set, more than L2); no flush",
+                      "dtype": "f32", "data": "synthetic (seeded, drawn on the device)"}), flush=True)
 
 
 def main(argv=None):
@@ -1012,6 +1098,7 @@ def main(argv=None):
                     help="instead of the step: the 4096-sample chunking workload in its five chunkings")
     ap.add_argument("--block", action="store_true",
                     help="instead of the step: the block-level modulated norm with a gated residual, fwd+bwd")
+    ap.add_argument("--fp32", action="store_true", help="instead of the step: the fp32 execution dtype's step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1024,6 +1111,9 @@ def main(argv=None):
         return
     if args.block:
         run_block(args, rank, local)
+        return
+    if args.fp32:
+        run_f32(args, rank, local)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)

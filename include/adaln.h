@@ -308,6 +308,73 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
                                    void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* FP32 execution dtype                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The same operator on fp32 tensors (RL-Kernel PR 538 "Results": the FP32
+ * timings and the BF16/FP32 acceptance gates): fp32 inputs and outputs, no
+ * bf16 rounding anywhere, each step of the eager fp32 graph rounded once to
+ * fp32, no TF32.  D is a multiple of 8 up to 4096; otherwise the conventions,
+ * checks and errors of the bf16 calls above.
+ *
+ * adaln_f32_proj_fwd:
+ *   u[b,k]   = fp32(silu(t))  (computed in fp64, rounded once)
+ *   emb[b,n] = fp32 sum_k u W + bias: lane l of a warp takes the 4-float
+ *              vectors l, l+32, ... of row n in ascending order, one fused
+ *              multiply-add per element, then a fixed xor butterfly; the
+ *              bias added in fp32.  The order depends on D only.
+ *   temb [B,D], W [2D,D], bias [2D] fp32 in;  emb [B,2D], u [B,D] fp32 out.
+ */
+adaln_status adaln_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B,
+                                int D, void *stream);
+
+/*
+ * adaln_f32_out_fwd:  per row, mean = sum / D, rstd = 1 / sqrt(sum (x -
+ * mean)^2 / D + eps) (fixed-order fp32 sums), xhat = fp32(fp32(x - mean) *
+ * rstd), onep = fp32(1 + scale), out = fp32(fp32(xhat * onep) + shift).
+ *   x [B,S,D], emb [B,2D] fp32 in;  out [B,S,D], mean, rstd [B,S] fp32 out.
+ */
+adaln_status adaln_f32_out_fwd(const float *x, const float *emb, float *out, float *mean, float *rstd, int B, int S,
+                               int D, float eps, void *stream);
+
+/* Workspace bytes adaln_f32_out_bwd needs (the tree nodes, as for adaln_out_bwd). */
+size_t adaln_f32_out_bwd_workspace_bytes(int B, int S, int D);
+
+/*
+ * adaln_f32_out_bwd:  g = dy, gh = fp32(g * onep); c1 = (sum_d fma g onep) / D,
+ * c2 = (sum_d fma p onep) / D with p = fp32(g * xhat); dx = fp32(rstd *
+ * ((gh - c1) - xhat * c2)), each operation rounded once; d_emb = [sum_s p |
+ * sum_s g] by the fixed 32-way token tree (as adaln_out_bwd, with xhat
+ * recomputed from the saved mean and rstd).
+ *   dy, x [B,S,D], emb [B,2D], mean, rstd [B,S] fp32 in;  dx [B,S,D], d_emb
+ *   [B,2D] fp32 out.
+ */
+adaln_status adaln_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
+                               const float *rstd, float *dx, float *d_emb, void *workspace, size_t workspace_bytes,
+                               int B, int S, int D, void *stream);
+
+/* Workspace bytes adaln_f32_proj_bwd needs: ceil(2D/256) * B * D fp32
+ * partials, rounded up to 256 bytes. */
+size_t adaln_f32_proj_bwd_workspace_bytes(int B, int D);
+
+/*
+ * adaln_f32_proj_bwd:  e = d_emb (no rounding);
+ *   d_temb[b,k] = fp32(d_silu * silu'(t)), d_silu = fp32 sum over n of e W in
+ *                 slabs of 256 rows (fused multiply-adds, rows ascending),
+ *                 the slabs added in ascending order; the product with
+ *                 silu'(t) in fp64, rounded once
+ *   dW_acc[n,k] : acc = accumulate ? dW_acc : +0; for b ascending:
+ *                 acc = fma(e[b,n], u[b,k], acc)   (one rounding per sample)
+ *   db_acc[n]   : the same with acc = acc + e[b,n]
+ *   d_emb [B,2D], temb, u [B,D], W [2D,D] fp32 in;  d_temb [B,D] out;
+ *   dW_acc [2D,D], db_acc [2D] fp32 in/out (either may be NULL).
+ */
+adaln_status adaln_f32_proj_bwd(const float *d_emb, const float *temb, const float *u, const float *W, float *d_temb,
+                                float *dW_acc, float *db_acc, int accumulate, void *workspace,
+                                size_t workspace_bytes, int B, int D, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Block-level modulated norm with a gated residual                           */
 /* ------------------------------------------------------------------------ */
 

@@ -41,6 +41,12 @@ _SIGNATURES = {
     "adaln_scale_residual_norm_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "adaln_scale_residual_norm_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I,
                                            _P]),
+    "adaln_f32_proj_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "adaln_f32_out_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P]),
+    "adaln_f32_out_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "adaln_f32_out_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _P]),
+    "adaln_f32_proj_bwd_workspace_bytes": (_SZ, [_I, _I]),
+    "adaln_f32_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _I, _I, _P]),
     "adaln_device_error": (_I, []),
 }
 
@@ -201,6 +207,80 @@ def adaln_out_bwd(dy, x, emb, mean, rstd, dx=None, d_emb=None, workspace=None, s
     _check("adaln_out_bwd", L.adaln_out_bwd(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd), _ptr(dx),
                                             _ptr(d_emb), _ptr(ws), nws, B, S, D, _stream(stream)))
     return dx, d_emb
+
+
+def adaln_f32_proj_fwd(temb, W, bias, emb=None, u=None, stream=None):
+    """fp32 projection: (emb [B,2D], u [B,D]), both fp32."""
+    L = load()
+    B, D = temb.shape
+    temb = _input(temb, torch.float32, (B, D), "temb")
+    W = _input(W, torch.float32, (2 * D, D), "W")
+    bias = _input(bias, torch.float32, (2 * D,), "bias")
+    emb = _output(emb, torch.float32, (B, 2 * D), "emb", temb.device)
+    u = _output(u, torch.float32, (B, D), "u", temb.device)
+    _check("adaln_f32_proj_fwd", L.adaln_f32_proj_fwd(_ptr(temb), _ptr(W), _ptr(bias), _ptr(emb), _ptr(u), B, D,
+                                                      _stream(stream)))
+    return emb, u
+
+
+def adaln_f32_out_fwd(x, emb, out=None, mean=None, rstd=None, eps=1e-6, stream=None):
+    """fp32 LayerNorm + modulation: (out [B,S,D], mean, rstd [B,S]), fp32."""
+    L = load()
+    B, S, D = x.shape
+    x = _input(x, torch.float32, (B, S, D), "x")
+    emb = _input(emb, torch.float32, (B, 2 * D), "emb")
+    out = _output(out, torch.float32, (B, S, D), "out", x.device)
+    mean = _output(mean, torch.float32, (B, S), "mean", x.device)
+    rstd = _output(rstd, torch.float32, (B, S), "rstd", x.device)
+    _check("adaln_f32_out_fwd", L.adaln_f32_out_fwd(_ptr(x), _ptr(emb), _ptr(out), _ptr(mean), _ptr(rstd), B, S, D,
+                                                    float(eps), _stream(stream)))
+    return out, mean, rstd
+
+
+def adaln_f32_out_bwd(dy, x, emb, mean, rstd, dx=None, d_emb=None, workspace=None, stream=None):
+    """fp32 backward of adaln_f32_out_fwd: (dx [B,S,D], d_emb [B,2D]), fp32."""
+    L = load()
+    B, S, D = x.shape
+    dy = _input(dy, torch.float32, (B, S, D), "dy")
+    x = _input(x, torch.float32, (B, S, D), "x")
+    emb = _input(emb, torch.float32, (B, 2 * D), "emb")
+    mean = _input(mean, torch.float32, (B, S), "mean")
+    rstd = _input(rstd, torch.float32, (B, S), "rstd")
+    dx = _output(dx, torch.float32, (B, S, D), "dx", x.device)
+    d_emb = _output(d_emb, torch.float32, (B, 2 * D), "d_emb", x.device)
+    ws, nws = _workspace(workspace, L.adaln_f32_out_bwd_workspace_bytes(B, S, D), x.device)
+    _check("adaln_f32_out_bwd", L.adaln_f32_out_bwd(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                                    _ptr(d_emb), _ptr(ws), nws, B, S, D, _stream(stream)))
+    return dx, d_emb
+
+
+def adaln_f32_out_bwd_workspace_bytes(B, S, D):
+    return load().adaln_f32_out_bwd_workspace_bytes(B, S, D)
+
+
+def adaln_f32_proj_bwd_workspace_bytes(B, D):
+    return load().adaln_f32_proj_bwd_workspace_bytes(B, D)
+
+
+def adaln_f32_proj_bwd(d_emb, temb, u, W, d_temb=None, dW_acc=None, db_acc=None, accumulate=False, want_w=True,
+                       workspace=None, stream=None):
+    """fp32 projection backward: (d_temb, dW_acc, db_acc); the accumulators are
+    allocated here when not given and want_w."""
+    L = load()
+    B, D = temb.shape
+    d_emb = _input(d_emb, torch.float32, (B, 2 * D), "d_emb")
+    temb = _input(temb, torch.float32, (B, D), "temb")
+    u = _input(u, torch.float32, (B, D), "u")
+    W = _input(W, torch.float32, (2 * D, D), "W")
+    d_temb = _output(d_temb, torch.float32, (B, D), "d_temb", temb.device)
+    if want_w:
+        dW_acc = _output(dW_acc, torch.float32, (2 * D, D), "dW_acc", temb.device)
+        db_acc = _output(db_acc, torch.float32, (2 * D,), "db_acc", temb.device)
+    ws, nws = _workspace(workspace, L.adaln_f32_proj_bwd_workspace_bytes(B, D), temb.device)
+    _check("adaln_f32_proj_bwd", L.adaln_f32_proj_bwd(_ptr(d_emb), _ptr(temb), _ptr(u), _ptr(W), _ptr(d_temb),
+                                                      _ptr(dW_acc), _ptr(db_acc), int(bool(accumulate)), _ptr(ws),
+                                                      nws, B, D, _stream(stream)))
+    return d_temb, dW_acc, db_acc
 
 
 def adaln_scale_residual_norm_fwd(x, residual, gate, emb, r=None, out=None, mean=None, rstd=None, eps=1e-6,

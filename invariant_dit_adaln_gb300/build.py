@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libadaln.so")
-SOURCES = ["api.cu", "out.cu", "proj.cu", "tc_proj.cu", "res.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "out.cu", "proj.cu", "tc_proj.cu", "res.cu", "f32.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xptxas", "-warn-spills", f"-I{INCLUDE}", f"-I{CSRC}"]

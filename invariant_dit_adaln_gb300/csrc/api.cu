@@ -249,6 +249,107 @@ adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H, vo
     return from_cuda(launch_token_tree(in, out, workspace, B, S, H, (cudaStream_t)stream, dev));
 }
 
+// ---- fp32 execution dtype (D <= 4096) ----
+
+adaln_status adaln_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B,
+                                int D, void *stream) {
+    if (!valid_D(D) || D > 4096 || B < 0 || B > (1 << 20)) return ADALN_ERR_SHAPE;
+    const size_t N = 2 * (size_t)D;
+    const Buf ins[] = {{temb, (size_t)B * D * 4}, {W, N * D * 4}, {bias, N * 4}};
+    const Buf outs[] = {{emb, (size_t)B * N * 4}, {u, (size_t)B * D * 4}};
+    if (any_missing(ins, 3) || any_missing(outs, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(temb) || !aligned16(W) || !aligned16(bias) || !aligned16(emb) || !aligned16(u))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 2, ins, 3)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_f32_proj_fwd(temb, W, bias, emb, u, B, D, (cudaStream_t)stream, dev));
+}
+
+adaln_status adaln_f32_out_fwd(const float *x, const float *emb, float *out, float *mean, float *rstd, int B, int S,
+                               int D, float eps, void *stream) {
+    if (!valid_D(D) || D > 4096 || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return ADALN_ERR_ARG;
+    const size_t rows = (size_t)B * S;
+    const Buf ins[] = {{x, rows * D * 4}, {emb, (size_t)B * 2 * D * 4}};
+    const Buf outs[] = {{out, rows * D * 4}, {mean, rows * 4}, {rstd, rows * 4}};
+    if (any_missing(ins, 2) || any_missing(outs, 3)) return ADALN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(emb) || !aligned16(out) || !aligned16(mean) || !aligned16(rstd))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 3, ins, 2)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (rows == 0) return ADALN_OK;
+    return from_cuda(launch_f32_out_fwd(x, emb, out, mean, rstd, B, S, D, eps, (cudaStream_t)stream, dev));
+}
+
+size_t adaln_f32_out_bwd_workspace_bytes(int B, int S, int D) { return adaln_out_bwd_workspace_bytes(B, S, D); }
+
+adaln_status adaln_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
+                               const float *rstd, float *dx, float *d_emb, void *workspace, size_t workspace_bytes,
+                               int B, int S, int D, void *stream) {
+    if (!valid_D(D) || D > 4096 || !valid_BS(B, S, D)) return ADALN_ERR_SHAPE;
+    const size_t rows = (size_t)B * S;
+    const size_t need = adaln_f32_out_bwd_workspace_bytes(B, S, D);
+    const Buf ins[] = {{dy, rows * D * 4}, {x, rows * D * 4}, {emb, (size_t)B * 2 * D * 4}, {mean, rows * 4},
+                       {rstd, rows * 4}};
+    const Buf outs[] = {{dx, rows * D * 4}, {d_emb, (size_t)B * 2 * D * 4}, {workspace, need}};
+    if (any_missing(ins, 5) || any_missing(outs, 2)) return ADALN_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(emb) || !aligned16(mean) || !aligned16(rstd) ||
+        !aligned16(dx) || !aligned16(d_emb) || !aligned16(workspace))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 3, ins, 5)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) return ADALN_OK;
+    return from_cuda(launch_f32_out_bwd(dy, x, emb, mean, rstd, dx, d_emb, workspace, B, S, D, (cudaStream_t)stream,
+                                        dev));
+}
+
+size_t adaln_f32_proj_bwd_workspace_bytes(int B, int D) {
+    if (B <= 0 || D <= 0) return 0;
+    return round256(f32_proj_bwd_ws_bytes(B, D));
+}
+
+adaln_status adaln_f32_proj_bwd(const float *d_emb, const float *temb, const float *u, const float *W, float *d_temb,
+                                float *dW_acc, float *db_acc, int accumulate, void *workspace,
+                                size_t workspace_bytes, int B, int D, void *stream) {
+    if (!valid_D(D) || D > 4096 || B < 0 || B > (1 << 20)) return ADALN_ERR_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return ADALN_ERR_ARG;
+    const size_t N = 2 * (size_t)D;
+    const size_t need = adaln_f32_proj_bwd_workspace_bytes(B, D);
+    const Buf ins[] = {{d_emb, (size_t)B * N * 4}, {temb, (size_t)B * D * 4}, {u, (size_t)B * D * 4},
+                       {W, N * D * 4}};
+    const Buf outs[] = {{d_temb, (size_t)B * D * 4}, {dW_acc, dW_acc ? N * D * 4 : 0},
+                        {db_acc, db_acc ? N * 4 : 0}, {workspace, need}};
+    if (any_missing(ins, 4) || any_missing(outs, 1)) return ADALN_ERR_NULL;
+    if (!aligned16(d_emb) || !aligned16(temb) || !aligned16(u) || !aligned16(W) || !aligned16(d_temb) ||
+        !aligned16(dW_acc) || !aligned16(db_acc) || !aligned16(workspace))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 4, ins, 4)) return ADALN_ERR_ALIAS;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return ADALN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (B == 0) {
+        // no samples: the gradient is its starting value (+0 unless accumulating)
+        if (!accumulate) {
+            cudaError_t e = cudaSuccess;
+            if (dW_acc) e = cudaMemsetAsync(dW_acc, 0, N * D * 4, (cudaStream_t)stream);
+            if (e == cudaSuccess && db_acc) e = cudaMemsetAsync(db_acc, 0, N * 4, (cudaStream_t)stream);
+            return from_cuda(e);
+        }
+        return ADALN_OK;
+    }
+    return from_cuda(launch_f32_proj_bwd(d_emb, temb, u, W, d_temb, dW_acc, db_acc, accumulate, workspace, B, D,
+                                         (cudaStream_t)stream, dev));
+}
+
 size_t adaln_scale_residual_norm_bwd_workspace_bytes(int B, int S, int D) {
     // the LayerNorm backward's tree nodes (2D columns), then the gate's (D
     // columns) in the same space

@@ -1,0 +1,460 @@
+// The operator in the fp32 execution dtype (RL-Kernel PR 538 "Results": the
+// FP32 timings and the BF16/FP32 acceptance gates): fp32 x, temb, W, bias, dy
+// and fp32 outputs, no bf16 rounding anywhere, every step one fp32 rounding
+// (no TF32: the tensor cores are not used).  The token trees and the weight
+// gradient's sequential order are the bf16 path's.
+//
+//   u      = fp32(silu(t))                     (fp64, rounded once)
+//   emb    = fp32 sum_k u W + bias             (fixed order: below)
+//   mean, rstd, xhat = fp32(fp32(x - mean) * rstd)
+//   out    = fp32(fp32(xhat * onep) + shift),  onep = fp32(1 + scale)
+//   dx     = rstd * (gh - c1 - xhat * c2),     gh = fp32(g * onep), g = dy
+//   d_emb  = the 32-way token trees of fp32(g * xhat) and g
+//   d_temb = fp32(d_silu * silu'(t)),          d_silu = sum_n e W, e = d_emb
+//   dW     = fma over samples ascending,        db = sum over samples ascending
+#include "common.cuh"
+#include "internal.h"
+
+namespace adaln {
+
+constexpr int kF32MaxD = 4096;  // the fp32 variant's largest row (a row per warp in registers)
+
+__device__ __forceinline__ float4 ldf4_hint(const float *p, uint64_t pol) {
+    const uint4 v = ldg16_hint(p, pol);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+// --------------------------------------------------------------------------
+// u = fp32(t / (1 + exp(-t))), computed in fp64 (B * D values)
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) f32_silu_kernel(const float *__restrict__ t, float *__restrict__ u, long long n) {
+    pdl_wait();
+    pdl_trigger();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const double x = (double)t[i];
+        u[i] = (float)(x * (1.0 / (1.0 + exp(-x))));
+    }
+}
+
+// --------------------------------------------------------------------------
+// emb[b,n] = sum_k u[b,k] W[n,k] + bias[n]: one warp per output row n; lane l
+// takes the float4 vectors l, l + 32, ... of the row in ascending order, the
+// four elements in order, one fused multiply-add each into one accumulator
+// per sample; then a fixed xor butterfly over the lanes and the bias in fp32.
+// The order depends on D only.  Samples in chunks of kF32BC (u of the chunk in
+// shared memory; W is read again for every chunk).
+// --------------------------------------------------------------------------
+constexpr int kF32BC = 4;
+
+__global__ void __launch_bounds__(256)
+f32_proj_fwd_kernel(const float *__restrict__ u, const float *__restrict__ W, const float *__restrict__ bias,
+                    float *__restrict__ emb, int B, int D) {
+    extern __shared__ __align__(16) float us_f32[];  // [kF32BC][D]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = 2 * D;
+    const int n = blockIdx.x * 8 + warp;
+    const bool live = n < N;
+    const int V = D / 4;
+    const float4 *wrow = reinterpret_cast<const float4 *>(W + (size_t)(live ? n : 0) * D);
+    pdl_wait();
+    pdl_trigger();
+    for (int b0 = 0; b0 < B; b0 += kF32BC) {
+        const int nb = min(kF32BC, B - b0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nb * V; i += blockDim.x)
+            reinterpret_cast<float4 *>(us_f32)[i] = reinterpret_cast<const float4 *>(u + (size_t)b0 * D)[i];
+        __syncthreads();
+        float acc[kF32BC];
+#pragma unroll
+        for (int b = 0; b < kF32BC; ++b) acc[b] = 0.0f;
+        for (int v0 = 0; v0 < V; v0 += 32 * 8) {
+            float4 w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int v = v0 + lane + 32 * j;
+                w[j] = v < V ? __ldg(wrow + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int v = v0 + lane + 32 * j;
+                if (v < V) {
+#pragma unroll
+                    for (int b = 0; b < kF32BC; ++b) {
+                        if (b < nb) {
+                            const float4 x = reinterpret_cast<const float4 *>(us_f32 + (size_t)b * D)[v];
+                            acc[b] = __fmaf_rn(x.x, w[j].x, acc[b]);
+                            acc[b] = __fmaf_rn(x.y, w[j].y, acc[b]);
+                            acc[b] = __fmaf_rn(x.z, w[j].z, acc[b]);
+                            acc[b] = __fmaf_rn(x.w, w[j].w, acc[b]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kF32BC; ++b) {
+            if (b < nb) {
+                const float tot = warp_sum(acc[b]);
+                if (lane == 0 && live) emb[(size_t)(b0 + b) * N + n] = __fadd_rn(tot, bias[n]);
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// LayerNorm + modulation forward: one warp per token row, rows of one sample
+// per CTA (onep and shift of the sample in shared memory).  Lane l holds the
+// float4 vectors l, l + 32, ... of the row in registers (D <= 4096).  Sums:
+// per lane in vector order, the four elements in order, then the xor
+// butterfly; mean = sum / D, var = sum (x - mean)^2 / D, rstd = 1 / sqrt(var
+// + eps), each operation rounded once.
+// --------------------------------------------------------------------------
+constexpr int kF32FwdVPL = kF32MaxD / 128;  // 32 vectors per lane
+
+__global__ void __launch_bounds__(256)
+f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, float *__restrict__ out,
+                   float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int rows_per_cta) {
+    extern __shared__ __align__(16) float tab_f32[];  // onep [D], shift [D]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int V = D / 4;
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        tab_f32[i] = __fadd_rn(1.0f, emb[(size_t)b * 2 * D + i]);
+        tab_f32[D + i] = emb[(size_t)b * 2 * D + D + i];
+    }
+    __syncthreads();
+    const float4 *po = reinterpret_cast<const float4 *>(tab_f32);
+    const float4 *ps = reinterpret_cast<const float4 *>(tab_f32 + D);
+    const float Df = (float)D;
+    const int s_begin = blockIdx.x * rows_per_cta;
+    const int s_end = min(S, s_begin + rows_per_cta);
+    const uint64_t pol = l2_evict_first();
+    for (int s = s_begin + warp; s < s_end; s += 8) {
+        const size_t row = (size_t)b * S + s;
+        const float *xr = x + row * D;
+        float4 xv[kF32FwdVPL];
+#pragma unroll
+        for (int j = 0; j < kF32FwdVPL; ++j) {
+            const int v = lane + 32 * j;
+            xv[j] = v < V ? ldf4_hint(xr + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        float s1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kF32FwdVPL; ++j)
+            if (lane + 32 * j < V)
+                s1 = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s1, xv[j].x), xv[j].y), xv[j].z), xv[j].w);
+        const float mu = __fdiv_rn(warp_sum(s1), Df);
+        auto sq = [&](float a, float acc) {
+            const float d = __fsub_rn(a, mu);
+            return __fadd_rn(acc, __fmul_rn(d, d));
+        };
+        float s2 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kF32FwdVPL; ++j)
+            if (lane + 32 * j < V) s2 = sq(xv[j].w, sq(xv[j].z, sq(xv[j].y, sq(xv[j].x, s2))));
+        const float var = __fdiv_rn(warp_sum(s2), Df);
+        const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+        if (lane == 0) {
+            mean[row] = mu;
+            rstd[row] = rs;
+        }
+        float4 *orow = reinterpret_cast<float4 *>(out + row * D);
+        auto mod = [&](float a, float on, float sh) {
+            return __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(a, mu), rs), on), sh);
+        };
+#pragma unroll
+        for (int j = 0; j < kF32FwdVPL; ++j) {
+            const int v = lane + 32 * j;
+            if (v < V) {
+                const float4 a = xv[j], on = po[v], sh = ps[v];
+                stg16f_hint(orow + v, make_float4(mod(a.x, on.x, sh.x), mod(a.y, on.y, sh.y), mod(a.z, on.z, sh.z),
+                                                  mod(a.w, on.w, sh.w)),
+                            pol);
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// LayerNorm + modulation backward and the level-0 tree tiles: one CTA per
+// (sample b, 32-token tile t); thread i owns the float4 vector i (D <= 4096:
+// at most 1024 threads).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
+// p = fp32(g * xhat) and g go into the columns' tiles by TwoSum from (+0, +0);
+// each thread's fused multiply-add sums of g * onep and p * onep over its
+// columns, the warp butterfly, the warps in ascending order: c1, c2 (divided
+// by D); dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(xhat * c2))).
+// --------------------------------------------------------------------------
+constexpr int VPT = 1;
+
+__global__ void __launch_bounds__(1024)
+f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ x, const float *__restrict__ emb,
+                        const float *__restrict__ mean, const float *__restrict__ rstd, float *__restrict__ dx,
+                        float *__restrict__ ws_sig, float *__restrict__ ws_kap, int S, int D, int T) {
+    __shared__ float2 red[2][32];
+    const int tid = threadIdx.x;
+    const int NT = blockDim.x;
+    const int nw = NT >> 5;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int t = blockIdx.x;
+    const int b = blockIdx.y;
+    const int V = D / 4;
+    const int H = 2 * D;
+    pdl_wait();
+    pdl_trigger();
+    float4 onep[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + NT * j;
+        if (v < V) {
+            const float4 sc = reinterpret_cast<const float4 *>(emb + (size_t)b * 2 * D)[v];
+            onep[j] = make_float4(__fadd_rn(1.0f, sc.x), __fadd_rn(1.0f, sc.y), __fadd_rn(1.0f, sc.z),
+                                  __fadd_rn(1.0f, sc.w));
+        } else {
+            onep[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    }
+    float ss[VPT][4], ks[VPT][4], sh[VPT][4], kh[VPT][4];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ss[j][c] = ks[j][c] = sh[j][c] = kh[j][c] = 0.0f;
+    const int s0 = t * kTile;
+    const int n = min(kTile, S - s0);
+    const float Df = (float)D;
+    const uint64_t pol = l2_evict_first();
+    float4 xn[VPT], gn[VPT];
+    auto load = [&](int i, float4 (&xa)[VPT], float4 (&ga)[VPT]) {
+        const size_t row = (size_t)b * S + s0 + i;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + NT * j;
+            xa[j] = v < V ? ldf4_hint(x + row * D + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            ga[j] = v < V ? ldf4_hint(dy + row * D + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    };
+    if (n > 0) load(0, xn, gn);
+    for (int i = 0; i < n; ++i) {
+        float4 xc[VPT], gc[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) xc[j] = xn[j], gc[j] = gn[j];
+        if (i + 1 < n) load(i + 1, xn, gn);  // the next row in flight
+        const size_t row = (size_t)b * S + s0 + i;
+        const float mu = mean[row], rs = rstd[row];
+        float a1 = 0.0f, a2 = 0.0f;
+        float xh[VPT][4];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            if (tid + NT * j < V) {
+                const float xe[4] = {xc[j].x, xc[j].y, xc[j].z, xc[j].w};
+                const float ge[4] = {gc[j].x, gc[j].y, gc[j].z, gc[j].w};
+                const float oe[4] = {onep[j].x, onep[j].y, onep[j].z, onep[j].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    xh[j][c] = __fmul_rn(__fsub_rn(xe[c], mu), rs);
+                    const float p = __fmul_rn(ge[c], xh[j][c]);
+                    twosum(ss[j][c], ks[j][c], p);
+                    twosum(sh[j][c], kh[j][c], ge[c]);
+                    a1 = __fmaf_rn(ge[c], oe[c], a1);
+                    a2 = __fmaf_rn(p, oe[c], a2);
+                }
+            }
+        }
+        a1 = warp_sum(a1);
+        a2 = warp_sum(a2);
+        if (lane == 0) red[i & 1][warp] = make_float2(a1, a2);
+        __syncthreads();
+        float t1 = red[i & 1][0].x, t2 = red[i & 1][0].y;
+        for (int w = 1; w < nw; ++w) t1 = __fadd_rn(t1, red[i & 1][w].x), t2 = __fadd_rn(t2, red[i & 1][w].y);
+        const float c1 = __fdiv_rn(t1, Df), c2 = __fdiv_rn(t2, Df);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + NT * j;
+            if (v < V) {
+                const float ge[4] = {gc[j].x, gc[j].y, gc[j].z, gc[j].w};
+                const float oe[4] = {onep[j].x, onep[j].y, onep[j].z, onep[j].w};
+                float o[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float gh = __fmul_rn(ge[c], oe[c]);
+                    o[c] = __fmul_rn(rs, __fsub_rn(__fsub_rn(gh, c1), __fmul_rn(xh[j][c], c2)));
+                }
+                stg16f_hint(dx + row * D + (size_t)v * 4, make_float4(o[0], o[1], o[2], o[3]), pol);
+            }
+        }
+        // red[i & 1] is written again two rows later, after the next barrier
+    }
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + NT * j;
+        if (v < V) {
+            const size_t node = ((size_t)b * T + t) * H + (size_t)v * 4;
+            stg16f(ws_sig + node, make_float4(ss[j][0], ss[j][1], ss[j][2], ss[j][3]));
+            stg16f(ws_kap + node, make_float4(ks[j][0], ks[j][1], ks[j][2], ks[j][3]));
+            stg16f(ws_sig + node + D, make_float4(sh[j][0], sh[j][1], sh[j][2], sh[j][3]));
+            stg16f(ws_kap + node + D, make_float4(kh[j][0], kh[j][1], kh[j][2], kh[j][3]));
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Projection backward: one CTA per (256 columns, 256-row slab of W), thread =
+// column k.  Over the slab's rows n ascending: d_silu partials
+// ds[b] = fma(e[b,n], W[n,k], ds[b]) (written per slab: ws[slab][b][k]), and
+// the weight gradient acc = fma(e[b,n], u[b,k], acc) over the samples
+// ascending, starting from the accumulator (accumulate) or +0; db likewise
+// with additions.  Samples in chunks of kF32BC; a later chunk continues from
+// the accumulator the earlier one wrote.
+// --------------------------------------------------------------------------
+constexpr int kF32Slab = 256;
+
+__global__ void __launch_bounds__(256)
+f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restrict__ u, const float *__restrict__ W,
+                         float *__restrict__ dW_acc, float *__restrict__ db_acc, int accumulate,
+                         float *__restrict__ ws, int B, int D) {
+    __shared__ float es[kF32BC][kF32Slab];
+    const int k = blockIdx.x * 256 + threadIdx.x;
+    const int slab = blockIdx.y;
+    const int N = 2 * D;
+    const int n0 = slab * kF32Slab;
+    const int rows = min(kF32Slab, N - n0);
+    const bool live = k < D;
+    pdl_wait();
+    pdl_trigger();
+    for (int b0 = 0; b0 < B; b0 += kF32BC) {
+        const int nb = min(kF32BC, B - b0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kF32BC * kF32Slab; i += blockDim.x) {
+            const int bb = i / kF32Slab, r = i % kF32Slab;
+            es[bb][r] = (bb < nb && r < rows) ? d_emb[(size_t)(b0 + bb) * N + n0 + r] : 0.0f;
+        }
+        __syncthreads();
+        float uk[kF32BC], ds[kF32BC];
+#pragma unroll
+        for (int bb = 0; bb < kF32BC; ++bb) {
+            uk[bb] = (live && bb < nb) ? u[(size_t)(b0 + bb) * D + k] : 0.0f;
+            ds[bb] = 0.0f;
+        }
+        const bool first = b0 == 0 && !accumulate;
+        for (int r0 = 0; r0 < rows; r0 += 8) {
+            float w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                w[q] = (live && r0 + q < rows) ? __ldg(W + (size_t)(n0 + r0 + q) * D + k) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int r = r0 + q;
+                if (r < rows) {
+#pragma unroll
+                    for (int bb = 0; bb < kF32BC; ++bb)
+                        if (bb < nb) ds[bb] = __fmaf_rn(es[bb][r], w[q], ds[bb]);
+                    if (dW_acc && live) {
+                        float *pa = dW_acc + (size_t)(n0 + r) * D + k;
+                        float a = first ? 0.0f : *pa;
+#pragma unroll
+                        for (int bb = 0; bb < kF32BC; ++bb)
+                            if (bb < nb) a = __fmaf_rn(es[bb][r], uk[bb], a);
+                        *pa = a;
+                    }
+                }
+            }
+        }
+        if (db_acc && blockIdx.x == 0)
+            for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+                float a = first ? 0.0f : db_acc[n0 + r];
+                for (int bb = 0; bb < nb; ++bb) a = __fadd_rn(a, es[bb][r]);
+                db_acc[n0 + r] = a;
+            }
+        if (live)
+#pragma unroll
+            for (int bb = 0; bb < kF32BC; ++bb)
+                if (bb < nb) __stcg(ws + ((size_t)slab * B + b0 + bb) * D + k, ds[bb]);
+    }
+}
+
+// d_temb[b,k] = fp32((sum over slabs, ascending) * silu'(t)), the product in fp64
+__global__ void __launch_bounds__(256)
+f32_proj_bwd_final_kernel(const float *__restrict__ ws, const float *__restrict__ temb, float *__restrict__ d_temb,
+                          int B, int D, int nslab) {
+    pdl_wait();
+    pdl_trigger();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long BD = (long long)B * D;
+    if (i < BD) {
+        float tot = __ldcg(ws + i);
+        for (int s = 1; s < nslab; ++s) tot = __fadd_rn(tot, __ldcg(ws + (size_t)s * BD + i));
+        const double x = (double)temb[i];
+        const double sg = 1.0 / (1.0 + exp(-x));
+        d_temb[i] = (float)((double)tot * (sg * (1.0 + x * (1.0 - sg))));
+    }
+}
+
+// --------------------------------------------------------------------------
+// launchers
+// --------------------------------------------------------------------------
+cudaError_t launch_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B,
+                                int D, cudaStream_t stream, const DeviceInfo &dev) {
+    const long long n = (long long)B * D;
+    cudaError_t err = launch_pdl(f32_silu_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, temb, u, n);
+    if (err != cudaSuccess) return err;
+    const size_t smem = (size_t)kF32BC * D * 4;
+    err = ensure_smem_attr((const void *)f32_proj_fwd_kernel, smem, dev);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(f32_proj_fwd_kernel, dim3((unsigned)((2 * D + 7) / 8)), dim3(256), smem, stream, u, W, bias,
+                      emb, B, D);
+}
+
+cudaError_t launch_f32_out_fwd(const float *x, const float *emb, float *out, float *mean, float *rstd, int B, int S,
+                               int D, float eps, cudaStream_t stream, const DeviceInfo &dev) {
+    const size_t smem = (size_t)2 * D * 4;
+    // about four CTAs of 8 warps per SM over the batch
+    int cps = (dev.sm_count * 4 + B - 1) / B;
+    if (cps > (S + 7) / 8) cps = (S + 7) / 8;
+    if (cps < 1) cps = 1;
+    const int rows = (S + cps - 1) / cps;
+    const dim3 grid((unsigned)((S + rows - 1) / rows), (unsigned)B);
+    cudaError_t err = ensure_smem_attr((const void *)f32_out_fwd_kernel, smem, dev);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(f32_out_fwd_kernel, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D, eps, rows);
+}
+
+cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
+                               const float *rstd, float *dx, float *d_emb, void *ws, int B, int S, int D,
+                               cudaStream_t stream, const DeviceInfo &dev) {
+    if (S == 0) return launch_zero(d_emb, (size_t)B * 2 * D, stream);
+    const int T = (S + kTile - 1) / kTile;
+    const int H = 2 * D;
+    float *sig = static_cast<float *>(ws);
+    float *kap = sig + (size_t)B * T * H;
+    const int nt = (D / 4 + 31) / 32 * 32;
+    cudaError_t err = launch_pdl(f32_out_bwd_tile_kernel, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
+                                 emb, mean, rstd, dx, sig, kap, S, D, T);
+    if (err != cudaSuccess) return err;
+    return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
+}
+
+size_t f32_proj_bwd_ws_bytes(int B, int D) {
+    const size_t nslab = (size_t)(2 * D + kF32Slab - 1) / kF32Slab;
+    return nslab * (size_t)B * D * 4;
+}
+
+cudaError_t launch_f32_proj_bwd(const float *d_emb, const float *temb, const float *u, const float *W,
+                                float *d_temb, float *dW_acc, float *db_acc, int accumulate, void *ws, int B, int D,
+                                cudaStream_t stream, const DeviceInfo &dev) {
+    (void)dev;
+    const int nslab = (2 * D + kF32Slab - 1) / kF32Slab;
+    float *part = static_cast<float *>(ws);
+    cudaError_t err = launch_pdl(f32_proj_bwd_slab_kernel, dim3((unsigned)((D + 255) / 256), (unsigned)nslab),
+                                 dim3(256), 0, stream, d_emb, u, W, dW_acc, db_acc, accumulate, part, B, D);
+    if (err != cudaSuccess) return err;
+    const long long BD = (long long)B * D;
+    return launch_pdl(f32_proj_bwd_final_kernel, dim3((unsigned)((BD + 255) / 256)), dim3(256), 0, stream, part, temb,
+                      d_temb, B, D, nslab);
+}
+
+}  // namespace adaln

@@ -67,6 +67,19 @@ cudaError_t launch_fold(const float *sig, const float *kap, float *out, int B, i
                         const DeviceInfo &dev);
 cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream);
 
+// f32.cu: the fp32 execution dtype (D <= 4096)
+cudaError_t launch_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B,
+                                int D, cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_f32_out_fwd(const float *x, const float *emb, float *out, float *mean, float *rstd, int B, int S,
+                               int D, float eps, cudaStream_t stream, const DeviceInfo &dev);
+cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
+                               const float *rstd, float *dx, float *d_emb, void *ws, int B, int S, int D,
+                               cudaStream_t stream, const DeviceInfo &dev);
+size_t f32_proj_bwd_ws_bytes(int B, int D);
+cudaError_t launch_f32_proj_bwd(const float *d_emb, const float *temb, const float *u, const float *W,
+                                float *d_temb, float *dW_acc, float *db_acc, int accumulate, void *ws, int B, int D,
+                                cudaStream_t stream, const DeviceInfo &dev);
+
 // res.cu: the block-level modulated norm with a gated residual
 cudaError_t launch_res_fwd(const uint16_t *x, const uint16_t *residual, const uint16_t *gate, const uint16_t *emb,
                            uint16_t *r, uint16_t *out, float *mean, float *rstd, int B, int S, int D, float eps,

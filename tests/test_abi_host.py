@@ -41,7 +41,7 @@ def fake(i, off=0):
 
 def test_library_exports_every_declared_symbol(L):
     names = binding.declared_symbols()
-    assert len(names) == 16, names
+    assert len(names) == 22, names
     for n in names:
         assert hasattr(L, n), n
     assert L.adaln_version() >> 16 == 1
@@ -252,6 +252,38 @@ def test_scale_residual_norm_checks(L, no_gpu):
     assert res_bwd(L, d_gate=fake(12, 0)) == ALIAS        # d_gate inside the workspace
     assert res_bwd(L, nws=16) == WORKSPACE
     assert res_bwd(L) == DEVICE
+
+
+# --- fp32 execution dtype ------------------------------------------------------
+
+def test_f32_checks(L, no_gpu):
+    F = ctypes.c_float
+    # projection forward: D <= 4096
+    assert L.adaln_f32_proj_fwd(fake(0), fake(1), fake(2), fake(3), fake(4), 2, 8192, None) == SHAPE
+    assert L.adaln_f32_proj_fwd(fake(0), None, fake(2), fake(3), fake(4), 2, 3072, None) == NULL
+    assert L.adaln_f32_proj_fwd(fake(0), fake(1), fake(2), fake(3, 4), fake(4), 2, 3072, None) == ALIGN
+    assert L.adaln_f32_proj_fwd(fake(0), fake(1), fake(2), fake(1, 64), fake(4), 2, 3072, None) == ALIAS
+    assert L.adaln_f32_proj_fwd(fake(0), fake(1), fake(2), fake(3), fake(4), 2, 3072, None) == DEVICE
+    # LayerNorm forward
+    assert L.adaln_f32_out_fwd(fake(0), fake(1), fake(2), fake(3), fake(4), 2, 33, 4104, F(1e-6), None) == SHAPE
+    assert L.adaln_f32_out_fwd(fake(0), fake(1), fake(2), fake(3), fake(4), 2, 33, 3072, F(-1.0), None) == ARG
+    assert L.adaln_f32_out_fwd(fake(0), fake(1), fake(0, 16), fake(3), fake(4), 2, 33, 3072, F(1e-6), None) == ALIAS
+    assert L.adaln_f32_out_fwd(fake(0), fake(1), fake(2), fake(3), fake(4), 2, 33, 3072, F(1e-6), None) == DEVICE
+    # backward
+    nws = L.adaln_f32_out_bwd_workspace_bytes(2, 33, 3072)
+    assert nws == L.adaln_out_bwd_workspace_bytes(2, 33, 3072)
+    args = [fake(i) for i in range(7)]
+    assert L.adaln_f32_out_bwd(*args, fake(7), nws, 2, 33, 3072, None) == DEVICE
+    assert L.adaln_f32_out_bwd(*args, fake(7), 8, 2, 33, 3072, None) == WORKSPACE
+    assert L.adaln_f32_out_bwd(*args[:5], fake(0, 32), args[6], fake(7), nws, 2, 33, 3072, None) == ALIAS
+    # projection backward
+    nws = L.adaln_f32_proj_bwd_workspace_bytes(2, 3072)
+    assert nws == 24 * 2 * 3072 * 4
+    p = [fake(i) for i in range(7)]
+    assert L.adaln_f32_proj_bwd(*p, 2, fake(7), nws, 2, 3072, None) == ARG
+    assert L.adaln_f32_proj_bwd(*p, 0, fake(7), nws, 2, 3072, None) == DEVICE
+    assert L.adaln_f32_proj_bwd(*p[:5], None, None, 0, fake(7), nws, 2, 3072, None) == DEVICE  # d_temb only
+    assert L.adaln_f32_proj_bwd(*p[:5], fake(3, 64), p[6], 0, fake(7), nws, 2, 3072, None) == ALIAS
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="a valid call with fake pointers would launch on a GPU")
