@@ -1080,6 +1080,87 @@ def run_f32(args, rank, local):
                       "dtype": "f32", "data": "synthetic (seeded, drawn on the device)"}), flush=True)
 
 
+def run_proj_out(args, rank, local):
+    """The forward with proj_out fused (adaln_out_fwd_proj) against the forward
+    alone (adaln_out_fwd) at B=2, S=4096, D=3072, J=64: K calls of each
+    replayed from CUDA graphs over two input sets larger than L2, median of
+    passes; one JSON line on rank 0 with tokens/s of the fused call, the time
+    y adds, and the fused call's algorithmic bytes (x read, out and y written,
+    mean/rstd, Wp) against the measured copy peak."""
+    if rank != 0:
+        return
+    import torch
+    from invariant_dit_adaln_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    build.build()
+    binding.load()
+    B, S, D, J = 2, 4096, 3072, 64
+    g = torch.Generator(device="cuda")
+    g.manual_seed(WORKLOAD["seed"])
+    Wp = (torch.randn((J, D), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    bp = (torch.randn((J,), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+
+    def make():
+        t = {"x": torch.randn((B, S, D), generator=g, device="cuda").to(torch.bfloat16),
+             "emb": (torch.randn((B, 2 * D), generator=g, device="cuda") * 0.3).to(torch.bfloat16)}
+        t["out"] = torch.empty((B, S, D), dtype=torch.bfloat16, device="cuda")
+        t["y"] = torch.empty((B, S, J), dtype=torch.bfloat16, device="cuda")
+        t["mean"], t["rstd"] = torch.empty((B, S), device="cuda"), torch.empty((B, S), device="cuda")
+        return t
+
+    sets = [make(), make()]
+    stream = torch.cuda.Stream()
+
+    def fused(t):
+        binding.adaln_out_fwd_proj(t["x"], t["emb"], Wp, bp, out=t["out"], mean=t["mean"], rstd=t["rstd"], y=t["y"],
+                                   stream=stream)
+
+    def alone(t):
+        binding.adaln_out_fwd(t["x"], t["emb"], out=t["out"], mean=t["mean"], rstd=t["rstd"], stream=stream)
+
+    res = {}
+    for name, fn in (("fused", fused), ("alone", alone)):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                for t in sets:
+                    fn(t)
+        torch.cuda.synchronize()
+        graphs = []
+        for t in sets:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn(t)
+            graphs.append(gr)
+        torch.cuda.synchronize()
+        K = min(args.steps, 2000)
+        passes = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for i in range(K):
+                    graphs[i % 2].replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            passes.append(e0.elapsed_time(e1) / K)
+        res[name] = statistics.median(passes)
+    if binding.device_error() != 0:
+        raise RuntimeError("device-side error in the proj_out workload")
+    ms = res["fused"]
+    alg = B * S * (2 * D * 2 + 8 + J * 2) + J * D * 2 + B * 2 * D * 2
+    peak, peak_src = hbm_peak()
+    print(json.dumps({"workload": "forward with proj_out fused (D -> 64), B=2 S=4096 D=3072",
+                      "value": B * S / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
+                      "ms_forward_alone": res["alone"], "ms_added_by_proj_out": ms - res["alone"],
+                      "algorithmic_bytes_per_call": alg, "hbm_gbs": alg / (ms / 1e3) / 1e9,
+                      "hbm_frac": alg / (ms / 1e3) / 1e9 / peak, "peak_gbs": peak, "peak_source": peak_src,
+                      "tflops_proj_out": 2.0 * B * S * D * J / ((ms - res["alone"]) / 1e3) / 1e12
+                      if ms > res["alone"] else None,
+                      "kernels_per_call": 2, "l2": "two input sets alternate (x 50.3 MB each); no flush",
+                      "data": "synthetic (seeded, drawn on the device)"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1099,6 +1180,7 @@ def main(argv=None):
     ap.add_argument("--block", action="store_true",
                     help="instead of the step: the block-level modulated norm with a gated residual, fwd+bwd")
     ap.add_argument("--fp32", action="store_true", help="instead of the step: the fp32 execution dtype's step")
+    ap.add_argument("--proj-out", action="store_true", help="instead of the step: the forward with proj_out fused")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1114,6 +1196,9 @@ def main(argv=None):
         return
     if args.fp32:
         run_f32(args, rank, local)
+        return
+    if args.proj_out:
+        run_proj_out(args, rank, local)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)

@@ -307,6 +307,30 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
                                    float *db_acc, adaln_bf16 *dW, adaln_bf16 *db, int accumulate, int B, int D,
                                    void *stream);
 
+/*
+ * adaln_out_fwd_proj — the forward of adaln_out_fwd with the model's next
+ * operation, proj_out (the latent projection D -> J = 64 that RL-Kernel PR 538
+ * "What" leaves to latent_proj_gemm), in the same call:
+ *
+ *   out, mean, rstd = adaln_out_fwd(x, emb)        (bits identical to it)
+ *   y[b,s,j] = bf16( sum_d out[b,s,d] * Wp[j,d]  +  bp[j] )
+ *
+ * The sum runs on the tensor cores (tcgen05.mma, 128 token rows x 64 x 16 per
+ * instruction, fp32 accumulation in tensor memory): k is cut into a number of
+ * contiguous ranges fixed by D (2 from D = 1024 on, else 1), each summed in
+ * ascending blocks of 16, the ranges added in order, then the bias, one bf16
+ * rounding.  A token's row of y depends only on its row of out.  out stays in
+ * L2 (evict-last) between the two kernels.
+ *
+ *   x [B,S,D], emb [B,2D], Wp [J,D], bp [J] bf16 in;  out [B,S,D], y [B,S,J]
+ *   bf16 and mean, rstd [B,S] fp32 out.  D a multiple of 64; J == 64;
+ *   B * S <= 65535 * 128.  Errors as adaln_out_fwd; ADALN_ERR_CUDA also when
+ *   the driver offers no tensor-map encoder.
+ */
+adaln_status adaln_out_fwd_proj(const adaln_bf16 *x, const adaln_bf16 *emb, const adaln_bf16 *Wp,
+                                const adaln_bf16 *bp, adaln_bf16 *out, float *mean, float *rstd, adaln_bf16 *y,
+                                int B, int S, int D, int J, float eps, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* FP32 execution dtype                                                       */
 /* ------------------------------------------------------------------------ */
@@ -453,7 +477,7 @@ adaln_status adaln_scale_residual_norm_bwd(const adaln_bf16 *d_out, const adaln_
  * a word instead of hanging, the kernel lets the copies it issued land, and it
  * returns without finishing its outputs.  Codes: 0x101 adaln_out_fwd, 0x201
  * adaln_out_bwd, 0x301 and 0x302 adaln_proj_fwd (CUDA-core and tensor-core
- * kernels); bit 0x8000 is or-ed in when an issued
+ * kernels), 0x303 adaln_out_fwd_proj; bit 0x8000 is or-ed in when an issued
  * copy did not land within the limit while the kernel was leaving.  Returns 0
  * when no kernel failed, -1 if a word could not be read.
  *

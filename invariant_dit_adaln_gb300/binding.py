@@ -47,6 +47,7 @@ _SIGNATURES = {
     "adaln_f32_out_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _P]),
     "adaln_f32_proj_bwd_workspace_bytes": (_SZ, [_I, _I]),
     "adaln_f32_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _I, _I, _P]),
+    "adaln_out_fwd_proj": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "adaln_device_error": (_I, []),
 }
 
@@ -207,6 +208,25 @@ def adaln_out_bwd(dy, x, emb, mean, rstd, dx=None, d_emb=None, workspace=None, s
     _check("adaln_out_bwd", L.adaln_out_bwd(_ptr(dy), _ptr(x), _ptr(emb), _ptr(mean), _ptr(rstd), _ptr(dx),
                                             _ptr(d_emb), _ptr(ws), nws, B, S, D, _stream(stream)))
     return dx, d_emb
+
+
+def adaln_out_fwd_proj(x, emb, Wp, bp, out=None, mean=None, rstd=None, y=None, eps=1e-6, stream=None):
+    """LayerNorm + modulation forward, then proj_out: y = bf16(out Wp^T + bp)
+    on the tensor cores.  Returns (out, mean, rstd, y)."""
+    L = load()
+    B, S, D = x.shape
+    J = Wp.shape[0]
+    x = _input(x, torch.bfloat16, (B, S, D), "x")
+    emb = _input(emb, torch.bfloat16, (B, 2 * D), "emb")
+    Wp = _input(Wp, torch.bfloat16, (J, D), "Wp")
+    bp = _input(bp, torch.bfloat16, (J,), "bp")
+    out = _output(out, torch.bfloat16, (B, S, D), "out", x.device)
+    mean = _output(mean, torch.float32, (B, S), "mean", x.device)
+    rstd = _output(rstd, torch.float32, (B, S), "rstd", x.device)
+    y = _output(y, torch.bfloat16, (B, S, J), "y", x.device)
+    _check("adaln_out_fwd_proj", L.adaln_out_fwd_proj(_ptr(x), _ptr(emb), _ptr(Wp), _ptr(bp), _ptr(out), _ptr(mean),
+                                                      _ptr(rstd), _ptr(y), B, S, D, J, float(eps), _stream(stream)))
+    return out, mean, rstd, y
 
 
 def adaln_f32_proj_fwd(temb, W, bias, emb=None, u=None, stream=None):

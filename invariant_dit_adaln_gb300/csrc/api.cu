@@ -249,6 +249,28 @@ adaln_status token_sum_tree(const float *in, float *out, int B, int S, int H, vo
     return from_cuda(launch_token_tree(in, out, workspace, B, S, H, (cudaStream_t)stream, dev));
 }
 
+adaln_status adaln_out_fwd_proj(const adaln_bf16 *x, const adaln_bf16 *emb, const adaln_bf16 *Wp,
+                                const adaln_bf16 *bp, adaln_bf16 *out, float *mean, float *rstd, adaln_bf16 *y,
+                                int B, int S, int D, int J, float eps, void *stream) {
+    if (!valid_D(D) || D % 64 != 0 || J != 64 || !valid_BS(B, S, D) || (long long)B * S > 65535LL * 128)
+        return ADALN_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return ADALN_ERR_ARG;
+    const size_t rows = (size_t)B * S;
+    const Buf ins[] = {{x, rows * D * 2}, {emb, (size_t)B * 2 * D * 2}, {Wp, (size_t)J * D * 2}, {bp, (size_t)J * 2}};
+    const Buf outs[] = {{out, rows * D * 2}, {mean, rows * 4}, {rstd, rows * 4}, {y, rows * J * 2}};
+    if (any_missing(ins, 4) || any_missing(outs, 4)) return ADALN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(emb) || !aligned16(Wp) || !aligned16(bp) || !aligned16(out) ||
+        !aligned16(mean) || !aligned16(rstd) || !aligned16(y))
+        return ADALN_ERR_ALIGN;
+    if (any_alias(outs, 4, ins, 4)) return ADALN_ERR_ALIAS;
+    DeviceInfo dev;
+    adaln_status st = current_device(&dev);
+    if (st != ADALN_OK) return st;
+    if (rows == 0) return ADALN_OK;
+    if (!proj_out_tc_supported(D, J)) return ADALN_ERR_CUDA;  // the driver offers no tensor-map encoder
+    return from_cuda(launch_out_fwd_proj(x, emb, Wp, bp, out, mean, rstd, y, B, S, D, eps, (cudaStream_t)stream, dev));
+}
+
 // ---- fp32 execution dtype (D <= 4096) ----
 
 adaln_status adaln_f32_proj_fwd(const float *temb, const float *W, const float *bias, float *emb, float *u, int B,

@@ -29,6 +29,7 @@ enum DeviceError : unsigned {
     kErrOutBwdWait = 0x201,
     kErrProjFwdWait = 0x301,
     kErrProjTcWait = 0x302,
+    kErrProjOutWait = 0x303,
     kErrDrainFailed = 0x8000,  // or-ed in: an issued copy did not land while leaving
 };
 

@@ -54,8 +54,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // out.cu
+// keep_out: write out as evict-last in L2 (a fused projection reads it next)
 cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean, float *rstd,
-                           int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev);
+                           int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev,
+                           bool keep_out = false);
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
                            cudaStream_t stream, const DeviceInfo &dev);
@@ -104,6 +106,12 @@ int proj_fwd_tc_ksplit(int D);
 cudaError_t launch_proj_fwd_tc(const uint16_t *u, const uint16_t *W, const uint16_t *bias, uint16_t *emb, int B,
                                int D, cudaStream_t stream, const DeviceInfo &dev);
 int read_and_clear_tc_error();
+// the LayerNorm forward, then y = out Wp^T + bp on the tensor cores (J = 64,
+// D a multiple of 64)
+bool proj_out_tc_supported(int D, int J);
+cudaError_t launch_out_fwd_proj(const uint16_t *x, const uint16_t *emb, const uint16_t *Wp, const uint16_t *bp,
+                                uint16_t *out, float *mean, float *rstd, uint16_t *y, int B, int S, int D,
+                                float eps, cudaStream_t stream, const DeviceInfo &dev);
 cudaError_t launch_wgrad_rows(const float *d_emb, const uint16_t *u, int n0, int n1, float *dW_acc, float *db_acc,
                               uint16_t *dW, uint16_t *db, int accumulate, int B, int D, cudaStream_t stream);
 

@@ -84,7 +84,8 @@ __device__ __forceinline__ bool wg_barrier_or(int id, bool flag) {
 template <int VPT, int BLK, int NST, int MINB>
 __global__ void __launch_bounds__(kWG * 128, MINB)
 out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
-               float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, long long R) {
+               float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, long long R,
+               int keep_out) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     FwdSmem &sm = *reinterpret_cast<FwdSmem *>(smem_raw);
     const int row_bytes = D * 2;
@@ -125,7 +126,8 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
     float2 onep[VPT][4], shift[VPT][4];  // modulation parameters of the current sample, by column pair
     long long cur_b = -1;
     const float Df = (float)D;
-    const uint64_t pol_out = l2_evict_first();  // out is not read again by this operator
+    // out is not read again by this operator, unless a fused projection reads it next
+    const uint64_t pol_out = keep_out ? l2_evict_last() : l2_evict_first();
 
     for (int r0 = 0; r0 < nrows; r0 += BLK) {
         const int nb = min(BLK, nrows - r0);
@@ -289,7 +291,8 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
 template <int VPL, int MAXW>
 __global__ void __launch_bounds__(MAXW * 32, 1)
 out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
-                   float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int cps, int NS) {
+                   float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int cps, int NS,
+                   int keep_out) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -359,7 +362,8 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     pdl_trigger();
 
     const float Df = (float)D;
-    const uint64_t pol_out = l2_evict_first();  // out is not read again by this operator
+    // out is not read again by this operator, unless a fused projection reads it next
+    const uint64_t pol_out = keep_out ? l2_evict_last() : l2_evict_first();
     for (int k = 0; k < nrows; ++k) {
         const size_t r = row0 + (size_t)k * NW;
         const int st = k % NS;
@@ -455,7 +459,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
 template <int VPL, int MAXW>
 static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean,
                                       float *rstd, int B, int S, int D, float eps, cudaStream_t stream,
-                                      const DeviceInfo &dev) {
+                                      const DeviceInfo &dev, bool keep_out) {
     constexpr size_t kSmemMax = 227 * 1024;
     auto smem_of = [&](int warps, int ns) { return 1024 + (size_t)D * 8 + (size_t)warps * ns * D * 2; };
     // 16 warps with 2 stages each where that fits, else 8 warps with 3 (or 2)
@@ -471,13 +475,13 @@ static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, ui
     if (cps < 1) cps = 1;
     const long long grid = (long long)B * cps;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(warps * 32), smem, stream, x, emb, out, mean, rstd, S, D, eps,
-                      cps, ns);
+                      cps, ns, keep_out ? 1 : 0);
 }
 
 template <int VPT, int BLK, int NST, int MINB>
 static cudaError_t launch_out_fwd_t(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean,
                                     float *rstd, int B, int S, int D, float eps, cudaStream_t stream,
-                                    const DeviceInfo &dev) {
+                                    const DeviceInfo &dev, bool keep_out) {
     static_assert(NST == 2 * BLK && BLK <= kFwdBlock, "two blocks of rows in flight");
     const size_t smem = ((sizeof(FwdSmem) + 127) / 128) * 128 + (size_t)kWG * NST * D * 2;
     auto kern = out_fwd_kernel<VPT, BLK, NST, MINB>;
@@ -492,26 +496,26 @@ static cudaError_t launch_out_fwd_t(const uint16_t *x, const uint16_t *emb, uint
     const long long need = (R + kWG - 1) / kWG;
     if (grid > need) grid = need;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kWG * 128), smem, stream,
-                      x, emb, out, mean, rstd, S, D, eps, R);
+                      x, emb, out, mean, rstd, S, D, eps, R, keep_out ? 1 : 0);
 }
 
 // Rows of up to 8 KB (D <= 4096): one warp per row.  Longer rows: the
 // warp-group kernel, with blocks of 2 rows and 4 stages (128 KB of stages).
 cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean, float *rstd,
-                           int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev) {
+                           int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev, bool keep_out) {
     const int V = D / 8;
-    if (V <= 128) return launch_out_fwd_row<4, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-    if (V <= 256) return launch_out_fwd_row<8, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-    if (V <= 384) return launch_out_fwd_row<12, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-    if (V <= 512) return launch_out_fwd_row<16, 8>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+    if (V <= 128) return launch_out_fwd_row<4, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+    if (V <= 256) return launch_out_fwd_row<8, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+    if (V <= 384) return launch_out_fwd_row<12, 16>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+    if (V <= 512) return launch_out_fwd_row<16, 8>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
     const int vpt = (V + 127) / 128;
     switch (vpt) {
-        case 1: return launch_out_fwd_t<1, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 2: return launch_out_fwd_t<2, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 3: return launch_out_fwd_t<3, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 4: return launch_out_fwd_t<4, 4, 8, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        case 5: case 6: return launch_out_fwd_t<6, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
-        default: return launch_out_fwd_t<8, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev);
+        case 1: return launch_out_fwd_t<1, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+        case 2: return launch_out_fwd_t<2, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+        case 3: return launch_out_fwd_t<3, 4, 8, 2>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+        case 4: return launch_out_fwd_t<4, 4, 8, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+        case 5: case 6: return launch_out_fwd_t<6, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
+        default: return launch_out_fwd_t<8, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
     }
 }
 

@@ -422,6 +422,219 @@ proj_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_const
 }
 
 // --------------------------------------------------------------------------
+// proj_out (the latent projection 3072 -> 64 after the final norm; RL-Kernel
+// PR 538 "What" leaves it to latent_proj_gemm) on the tensor cores, fused with
+// the LayerNorm forward in one call: the forward writes out as evict-last in
+// L2 and this kernel reads it back from there.
+//     y[r, j] = bf16( sum_d out[r, d] Wp[j, d]  +  bp[j] )
+// A tile is 128 token rows of out (MMA M) by the 64 rows of Wp (MMA N); k is
+// cut into kPoSplit(D) ranges (a cluster, partials added in range order in
+// the leading CTA), ascending blocks of 64 within a range, four tcgen05.mma of
+// 128 x 64 x 16 per block.  A token's row of y depends only on its own row of
+// out, so y does not depend on B, S or the token's position.
+// --------------------------------------------------------------------------
+constexpr int kPoN = 64;                              // rows of Wp (MMA N)
+constexpr int kPoKblk = 2;                            // k blocks per stage
+constexpr int kPoStages = 4;
+constexpr int kPoATile = kTcM * kTcK * 2;             // 16 KB of out
+constexpr int kPoBTile = kPoN * kTcK * 2;             // 8 KB of Wp
+constexpr int kPoStageBytes = kPoKblk * (kPoATile + kPoBTile);
+constexpr int kPoArea = kPoStages * kPoStageBytes;    // 192 KB
+constexpr size_t kPoSmemBytes = (size_t)kPoArea + 256 + 1024;
+constexpr uint32_t kPoIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPoN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+static_assert(kPoSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kPoN * kTcM * 4 <= kPoArea, "one partner's partials fit in the stage buffers");
+
+struct PoSmem {
+    uint64_t full[kPoStages];
+    uint64_t empty[kPoStages];
+    uint64_t done;
+    uint32_t tmem;
+    int abort;
+    int bad;
+};
+
+__global__ void __launch_bounds__(128, 1)
+proj_out_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const uint16_t *__restrict__ bp, uint16_t *__restrict__ y, int R, int D, int ksplit) {
+    extern __shared__ unsigned char po_smem_raw[];
+    const uint32_t raw = smem_u32(po_smem_raw);
+    unsigned char *stages = po_smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    PoSmem &sm = *reinterpret_cast<PoSmem *>(stages + kPoArea);
+    volatile int *abort_flag = &sm.abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int r0 = blockIdx.y * kTcM;
+    const int KB = D / kTcK;
+    const int kb0 = kb_begin(KB, ksplit, (int)rank);
+    const int nkb = kb_begin(KB, ksplit, (int)rank + 1) - kb0;
+    const int nst = (nkb + kPoKblk - 1) / kPoKblk;
+    constexpr uint32_t kb_tx = kPoATile + kPoBTile;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kPoStages; ++st) {
+            mbar_init(&sm.full[st], 1);
+            mbar_init(&sm.empty[st], 1);
+        }
+        mbar_init(&sm.done, 1);
+        sm.abort = 0;
+        sm.bad = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
+                     "r"(kPoN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = sm.tmem;
+    auto a_tile = [&](int st, int j) { return stages + st * kPoStageBytes + j * kPoATile; };
+    auto b_tile = [&](int st, int j) { return stages + st * kPoStageBytes + kPoKblk * kPoATile + j * kPoBTile; };
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer: Wp of the first stages before the wait (a call input;
+        // the LayerNorm kernel before this one waited for all earlier work),
+        // out after it ----
+        const uint64_t pol_a = l2_evict_first();  // out is read once more, here
+        const int first = min(kPoStages, nst);
+        for (int i = 0; i < first; ++i) {
+            const int nk = min(kPoKblk, nkb - i * kPoKblk);
+            mbar_arrive_expect_tx(&sm.full[i], (uint32_t)nk * kb_tx);
+            for (int j = 0; j < nk; ++j) tma_load_2d(b_tile(i, j), &map_b, (kb0 + i * kPoKblk + j) * kTcK, 0, &sm.full[i]);
+        }
+        pdl_wait();
+        for (int i = 0; i < first; ++i) {
+            const int nk = min(kPoKblk, nkb - i * kPoKblk);
+            for (int j = 0; j < nk; ++j)
+                tma_load_2d_hint(a_tile(i, j), &map_a, (kb0 + i * kPoKblk + j) * kTcK, r0, &sm.full[i], pol_a);
+        }
+        int issued = first;
+        for (int i = first; i < nst; ++i) {
+            const int st = i % kPoStages;
+            if (!mbar_wait_or_abort(&sm.empty[st], (uint32_t)(i / kPoStages - 1) & 1u, abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            const int nk = min(kPoKblk, nkb - i * kPoKblk);
+            mbar_arrive_expect_tx(&sm.full[st], (uint32_t)nk * kb_tx);
+            for (int j = 0; j < nk; ++j) {
+                const int kc = (kb0 + i * kPoKblk + j) * kTcK;
+                tma_load_2d(b_tile(st, j), &map_b, kc, 0, &sm.full[st]);
+                tma_load_2d_hint(a_tile(st, j), &map_a, kc, r0, &sm.full[st], pol_a);
+            }
+            issued = i + 1;
+        }
+        for (int st = 0; st < kPoStages && st < issued; ++st) {
+            const int last = st + kPoStages * ((issued - 1 - st) / kPoStages);
+            if (!mbar_wait_bounded(&sm.full[st], (uint32_t)(last / kPoStages) & 1u, 100000000ull))
+                report_error_tc(kErrDrainFailed);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        for (int i = 0; i < nst; ++i) {
+            const int st = i % kPoStages;
+            if (!mbar_wait_or_abort(&sm.full[st], (uint32_t)(i / kPoStages) & 1u, abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int nk = min(kPoKblk, nkb - i * kPoKblk);
+            for (int j = 0; j < nk; ++j) {
+                const uint64_t ad0 = tc_desc(smem_u32(a_tile(st, j))), bd0 = tc_desc(smem_u32(b_tile(st, j)));
+#pragma unroll
+                for (int k = 0; k < kTcK / 16; ++k) {
+                    const uint32_t accumulate = (i > 0 || j > 0 || k > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\t"
+                        "setp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                        "l"(ad0 + 2u * k), "l"(bd0 + 2u * k), "r"(kPoIdesc), "r"(accumulate)
+                        : "memory");
+                }
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_u32(&sm.empty[st]))
+                         : "memory");
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_u32(&sm.done))
+                     : "memory");
+    }
+    pdl_trigger();
+
+    bool ok = mbar_wait_or_abort(&sm.done, 0u, abort_flag) && !*abort_flag;
+    if (!ok && threadIdx.x == 0) {
+        report_error_tc(kErrProjOutWait);
+        if (!mbar_wait_bounded(&sm.done, 0u, 100000000ull)) report_error_tc(kErrDrainFailed);
+    }
+    ok = __syncthreads_and(ok);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // thread t holds token row r0 + t: columns 0..31 and 32..63 of the accumulator
+    uint32_t v[kPoN];
+    {
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t (&v0)[kTcN] = *reinterpret_cast<uint32_t(*)[kTcN]>(&v[0]);
+        uint32_t (&v1)[kTcN] = *reinterpret_cast<uint32_t(*)[kTcN]>(&v[kTcN]);
+        tmem_ld_tile(trow, v0);
+        tmem_ld_tile(trow + kTcN, v1);
+    }
+    float4 *part = reinterpret_cast<float4 *>(stages);  // [ksplit - 1][kPoN / 4][kTcM]
+    if (ksplit > 1) {
+        cluster_sync();
+        if (rank > 0) {
+            float4 *mine = part + (size_t)(rank - 1) * (kPoN / 4) * kTcM;
+#pragma unroll
+            for (int c = 0; c < kPoN / 4; ++c)
+                st_cluster_v4(map_to_rank(mine + c * kTcM + threadIdx.x, 0),
+                              make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
+            if (threadIdx.x == 0 && !ok) st_cluster_s32(map_to_rank(&sm.bad, 0), 1);
+        }
+        cluster_sync();
+    }
+    const int r = r0 + threadIdx.x;
+    if (rank == 0 && ok && sm.bad == 0 && r < R) {
+        float acc[kPoN];
+#pragma unroll
+        for (int c = 0; c < kPoN; ++c) acc[c] = __uint_as_float(v[c]);
+        for (int q = 1; q < ksplit; ++q) {
+            const float4 *theirs = part + (size_t)(q - 1) * (kPoN / 4) * kTcM;
+#pragma unroll
+            for (int c = 0; c < kPoN / 4; ++c) {
+                const float4 p = theirs[c * kTcM + threadIdx.x];
+                acc[4 * c] = __fadd_rn(acc[4 * c], p.x);
+                acc[4 * c + 1] = __fadd_rn(acc[4 * c + 1], p.y);
+                acc[4 * c + 2] = __fadd_rn(acc[4 * c + 2], p.z);
+                acc[4 * c + 3] = __fadd_rn(acc[4 * c + 3], p.w);
+            }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(y + (size_t)r * kPoN);
+#pragma unroll
+        for (int c = 0; c < kPoN / 8; ++c) {
+            const uint4 bw = ldg16(bp + 8 * c);
+            const uint32_t b4[4] = {bw.x, bw.y, bw.z, bw.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o[q] = pack_bf16x2(__fadd_rn(acc[8 * c + 2 * q], bf16lo(b4[q])),
+                                   __fadd_rn(acc[8 * c + 2 * q + 1], bf16hi(b4[q])));
+            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPoN) : "memory");
+    }
+}
+
+// --------------------------------------------------------------------------
 // host side
 // --------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -538,6 +751,42 @@ cudaError_t launch_proj_fwd_tc(const uint16_t *u, const uint16_t *W, const uint1
     cfg.attrs = attr;
     cfg.numAttrs = 3;
     return cudaLaunchKernelEx(&cfg, proj_fwd_tc_kernel, map_w, map_u, a);
+}
+
+// k ranges of proj_out: two (a cluster of 2) from 16 k blocks on, else one;
+// fixed by D alone
+static int proj_out_ksplit(int D) { return D / kTcK >= 16 ? 2 : 1; }
+
+bool proj_out_tc_supported(int D, int J) { return J == kPoN && D > 0 && D % kTcK == 0 && encode_fn() != nullptr; }
+
+cudaError_t launch_out_fwd_proj(const uint16_t *x, const uint16_t *emb, const uint16_t *Wp, const uint16_t *bp,
+                                uint16_t *out, float *mean, float *rstd, uint16_t *y, int B, int S, int D,
+                                float eps, cudaStream_t stream, const DeviceInfo &dev) {
+    const int R = B * S;
+    CUtensorMap map_a, map_b;
+    if (!make_map(&map_a, out, R, D, kTcM) || !make_map(&map_b, Wp, kPoN, D, kPoN)) return cudaErrorInvalidValue;
+    cudaError_t err = launch_out_fwd(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, true);
+    if (err != cudaSuccess) return err;
+    err = ensure_smem_attr((const void *)proj_out_tc_kernel, kPoSmemBytes, dev);
+    if (err != cudaSuccess) return err;
+    const int ks = proj_out_ksplit(D);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)((R + kTcM - 1) / kTcM), 1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kPoSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[3];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+    attr[1].val.sharedMemCarveout = (unsigned)cudaSharedmemCarveoutMaxShared;
+    attr[2].id = cudaLaunchAttributeClusterDimension;
+    attr[2].val.clusterDim.x = (unsigned)ks;
+    attr[2].val.clusterDim.y = 1;
+    attr[2].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 3;
+    return cudaLaunchKernelEx(&cfg, proj_out_tc_kernel, map_a, map_b, bp, y, R, D, ks);
 }
 
 int read_and_clear_tc_error() {

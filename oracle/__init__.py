@@ -75,6 +75,7 @@ def _load():
             "oracle_f32_bwd_products": [P, P, P, P, P, I, I, I],
             "oracle_f32_proj_bwd": [P, P, P, P, P, P, I, I],
             "oracle_f32_wgrad_seq": [P, P, P, P, I, I, I],
+            "oracle_proj_out": [P, P, P, P, Lg, I, I],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -325,6 +326,19 @@ def res_gate_products_f32(gr, x):
     prod = np.empty(x.shape, dtype=np.float32)
     _load().oracle_res_gate_products_f32(_p(gr), _p(x), _p(prod), x.size)
     return prod
+
+
+# --- proj_out ------------------------------------------------------------------
+
+def proj_out(out, Wp, bp):
+    """y [..., J] (bf16 bits) = bf16(out @ Wp^T + bp) for out [..., D] bf16 bits."""
+    out, Wp, bp = _c(out, np.uint16), _c(Wp, np.uint16), _c(bp, np.uint16)
+    J, D = Wp.shape
+    assert out.shape[-1] == D and bp.shape == (J,)
+    R = out.size // D
+    y = np.empty(out.shape[:-1] + (J,), dtype=np.uint16)
+    _load().oracle_proj_out(_p(out), _p(Wp), _p(bp), _p(y), R, D, J)
+    return y
 
 
 # --- fp32 execution dtype ----------------------------------------------------

@@ -822,6 +822,29 @@ void oracle_f32_wgrad_seq(const float *d_emb, const float *u, float *dW_acc, flo
 }
 
 /* ------------------------------------------------------------------------ */
+/* proj_out: the latent projection after the final norm (RL-Kernel PR 538    */
+/* "What": 3072 -> 64, latent_proj_gemm), on the bf16 output of the norm      */
+/* ------------------------------------------------------------------------ */
+
+/* y[r,j] = bf16(sum_d out[r,d] Wp[j,d] + bp[j]): the exact sum (compensated
+ * fp64 over the exact products), rounded once                               */
+void oracle_proj_out(const uint16_t *out, const uint16_t *Wp, const uint16_t *bp, uint16_t *y, long R, int D, int J)
+{
+    double *a = malloc(sizeof(double) * (size_t)D);
+    double *w = malloc(sizeof(double) * (size_t)J * D);
+    double *bb = malloc(sizeof(double) * (size_t)J);
+    double *e = malloc(sizeof(double) * (size_t)J);
+    for (size_t i = 0; i < (size_t)J * D; ++i) w[i] = bf16_to_f64(Wp[i]);
+    for (int j = 0; j < J; ++j) bb[j] = bf16_to_f64(bp[j]);
+    for (long r = 0; r < R; ++r) {
+        for (int d = 0; d < D; ++d) a[d] = bf16_to_f64(out[(size_t)r * D + d]);
+        proj_core(a, w, bb, e, 1, D, J, 0, J);
+        for (int j = 0; j < J; ++j) y[(size_t)r * J + j] = bf16_from_f64(e[j]);
+    }
+    free(a); free(w); free(bb); free(e);
+}
+
+/* ------------------------------------------------------------------------ */
 /* format helpers exported for the tests                                     */
 /* ------------------------------------------------------------------------ */
 

@@ -41,7 +41,7 @@ def fake(i, off=0):
 
 def test_library_exports_every_declared_symbol(L):
     names = binding.declared_symbols()
-    assert len(names) == 22, names
+    assert len(names) == 23, names
     for n in names:
         assert hasattr(L, n), n
     assert L.adaln_version() >> 16 == 1
@@ -252,6 +252,25 @@ def test_scale_residual_norm_checks(L, no_gpu):
     assert res_bwd(L, d_gate=fake(12, 0)) == ALIAS        # d_gate inside the workspace
     assert res_bwd(L, nws=16) == WORKSPACE
     assert res_bwd(L) == DEVICE
+
+
+# --- adaln_out_fwd_proj --------------------------------------------------------
+
+def test_out_fwd_proj_checks(L, no_gpu):
+    F = ctypes.c_float
+
+    def call(x=0, emb=1, Wp=2, bp=3, out=4, mean=5, rstd=6, y=7, B=2, S=33, D=3072, J=64, eps=1e-6):
+        p = [None if a is None else (fake(a) if isinstance(a, int) else a) for a in (x, emb, Wp, bp, out, mean, rstd, y)]
+        return L.adaln_out_fwd_proj(*p, B, S, D, J, F(eps), None)
+
+    assert call(J=32) == SHAPE
+    assert call(D=3080) == SHAPE           # not a multiple of 64
+    assert call(B=65535, S=262144) == SHAPE
+    assert call(eps=float("nan")) == ARG
+    assert call(Wp=None) == NULL
+    assert call(y=fake(7, 2)) == ALIGN
+    assert call(y=fake(4, 1024)) == ALIAS  # y inside out
+    assert call() == DEVICE
 
 
 # --- fp32 execution dtype ------------------------------------------------------

@@ -881,3 +881,29 @@ def test_f32_wgrad_seq_is_a_sequential_fused_multiply_add(orc):
     dW2, db2 = orc.f32_wgrad_seq(e[2:], u[2:], dW1, db1, accumulate=True)
     assert_bitwise(dW2, dW, "chunked dW")
     assert_bitwise(db2, db, "chunked db")
+
+
+# ---------------------------------------------------------------------------
+# proj_out (RL-Kernel PR 538 "What": the latent projection 3072 -> 64)
+# ---------------------------------------------------------------------------
+
+def test_proj_out_exact_rational_and_torch(orc):
+    """y = bf16(out Wp^T + bp): exact rational sums rounded once (bit for bit)
+    on a small case; the fp64 map against torch.nn.functional.linear; Wp = 0
+    gives y = bp; Wp's rows are the output features (a transposed Wp fails)."""
+    rng = np.random.default_rng(50)
+    R, D, J = 5, 16, 8
+    out = _bf16(rng.standard_normal((R, D)))
+    Wp = _bf16(rng.standard_normal((J, D)) * 0.1)
+    bp = _bf16(rng.standard_normal(J) * 0.1)
+    y = orc.proj_out(out, Wp, bp)
+    of, wf, bf = bf16_to_f64(out), bf16_to_f64(Wp), bf16_to_f64(bp)
+    for r in range(R):
+        for j in range(J):
+            v = sum(Fraction(float(of[r, d])) * Fraction(float(wf[j, d])) for d in range(D)) + Fraction(float(bf[j]))
+            assert int(y[r, j]) == bf16_exact_round(v), (r, j)
+    t = torch.nn.functional.linear(torch.tensor(of), torch.tensor(wf), torch.tensor(bf)).numpy()
+    assert np.all(bf16_ulp_dist(y, orc.bf16_from_f64(t)) <= 1)
+    assert_bitwise(orc.proj_out(out, np.zeros_like(Wp), bp), np.broadcast_to(bp, (R, J)).astype(np.uint16), "Wp = 0")
+    sq = _bf16(rng.standard_normal((D, D)) * 0.1)
+    assert not np.array_equal(orc.proj_out(out, sq, bp[:1].repeat(D)), orc.proj_out(out, sq.T.copy(), bp[:1].repeat(D)))
