@@ -111,9 +111,10 @@ f32_proj_fwd_kernel(const float *__restrict__ u, const float *__restrict__ W, co
 // butterfly; mean = sum / D, var = sum (x - mean)^2 / D, rstd = 1 / sqrt(var
 // + eps), each operation rounded once.
 // --------------------------------------------------------------------------
-constexpr int kF32FwdVPL = kF32MaxD / 128;  // 32 vectors per lane
+constexpr int kF32FwdVPL = kF32MaxD / 128;  // 32 vectors per lane at most
 
-__global__ void __launch_bounds__(256)
+template <int VPL>
+__global__ void __launch_bounds__(256, VPL <= 24 ? 2 : 1)
 f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, float *__restrict__ out,
                    float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int rows_per_cta) {
     extern __shared__ __align__(16) float tab_f32[];  // onep [D], shift [D]
@@ -137,15 +138,15 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
     for (int s = s_begin + warp; s < s_end; s += 8) {
         const size_t row = (size_t)b * S + s;
         const float *xr = x + row * D;
-        float4 xv[kF32FwdVPL];
+        float4 xv[VPL];
 #pragma unroll
-        for (int j = 0; j < kF32FwdVPL; ++j) {
+        for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
             xv[j] = v < V ? ldf4_hint(xr + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         float s1 = 0.0f;
 #pragma unroll
-        for (int j = 0; j < kF32FwdVPL; ++j)
+        for (int j = 0; j < VPL; ++j)
             if (lane + 32 * j < V)
                 s1 = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s1, xv[j].x), xv[j].y), xv[j].z), xv[j].w);
         const float mu = __fdiv_rn(warp_sum(s1), Df);
@@ -155,7 +156,7 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
         };
         float s2 = 0.0f;
 #pragma unroll
-        for (int j = 0; j < kF32FwdVPL; ++j)
+        for (int j = 0; j < VPL; ++j)
             if (lane + 32 * j < V) s2 = sq(xv[j].w, sq(xv[j].z, sq(xv[j].y, sq(xv[j].x, s2))));
         const float var = __fdiv_rn(warp_sum(s2), Df);
         const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
@@ -168,7 +169,7 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
             return __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(a, mu), rs), on), sh);
         };
 #pragma unroll
-        for (int j = 0; j < kF32FwdVPL; ++j) {
+        for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
             if (v < V) {
                 const float4 a = xv[j], on = po[v], sh = ps[v];
@@ -182,16 +183,16 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
 
 // --------------------------------------------------------------------------
 // LayerNorm + modulation backward and the level-0 tree tiles: one CTA per
-// (sample b, 32-token tile t); thread i owns the float4 vector i (D <= 4096:
-// at most 1024 threads).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
+// (sample b, 32-token tile t); thread i owns the float4 vectors i + NT j
+// (j < VPT: two per thread up to D = 3072, four up to 4096).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
 // p = fp32(g * xhat) and g go into the columns' tiles by TwoSum from (+0, +0);
 // each thread's fused multiply-add sums of g * onep and p * onep over its
 // columns, the warp butterfly, the warps in ascending order: c1, c2 (divided
-// by D); dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(xhat * c2))).
+// by D); dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(xhat * c2))).  Two CTAs
+// per SM hide the loads' latency.
 // --------------------------------------------------------------------------
-constexpr int VPT = 1;
-
-__global__ void __launch_bounds__(1024)
+template <int VPT>
+__global__ void __launch_bounds__(VPT == 2 ? 384 : 256, 2)
 f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ x, const float *__restrict__ emb,
                         const float *__restrict__ mean, const float *__restrict__ rstd, float *__restrict__ dx,
                         float *__restrict__ ws_sig, float *__restrict__ ws_kap, int S, int D, int T) {
@@ -228,7 +229,6 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
     const int n = min(kTile, S - s0);
     const float Df = (float)D;
     const uint64_t pol = l2_evict_first();
-    float4 xn[VPT], gn[VPT];
     auto load = [&](int i, float4 (&xa)[VPT], float4 (&ga)[VPT]) {
         const size_t row = (size_t)b * S + s0 + i;
 #pragma unroll
@@ -238,12 +238,9 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
             ga[j] = v < V ? ldf4_hint(dy + row * D + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
     };
-    if (n > 0) load(0, xn, gn);
     for (int i = 0; i < n; ++i) {
         float4 xc[VPT], gc[VPT];
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) xc[j] = xn[j], gc[j] = gn[j];
-        if (i + 1 < n) load(i + 1, xn, gn);  // the next row in flight
+        load(i, xc, gc);
         const size_t row = (size_t)b * S + s0 + i;
         const float mu = mean[row], rs = rstd[row];
         float a1 = 0.0f, a2 = 0.0f;
@@ -312,6 +309,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
 // the accumulator the earlier one wrote.
 // --------------------------------------------------------------------------
 constexpr int kF32Slab = 256;
+constexpr int kF32SlabRowsInFlight = 32;  // rows of W each thread has requested at once
 
 __global__ void __launch_bounds__(256)
 f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restrict__ u, const float *__restrict__ W,
@@ -341,13 +339,13 @@ f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restric
             ds[bb] = 0.0f;
         }
         const bool first = b0 == 0 && !accumulate;
-        for (int r0 = 0; r0 < rows; r0 += 8) {
-            float w[8];
+        for (int r0 = 0; r0 < rows; r0 += kF32SlabRowsInFlight) {
+            float w[kF32SlabRowsInFlight];  // requested before the first use
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < kF32SlabRowsInFlight; ++q)
                 w[q] = (live && r0 + q < rows) ? __ldg(W + (size_t)(n0 + r0 + q) * D + k) : 0.0f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < kF32SlabRowsInFlight; ++q) {
                 const int r = r0 + q;
                 if (r < rows) {
 #pragma unroll
@@ -386,8 +384,14 @@ f32_proj_bwd_final_kernel(const float *__restrict__ ws, const float *__restrict_
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
     if (i < BD) {
-        float tot = __ldcg(ws + i);
-        for (int s = 1; s < nslab; ++s) tot = __fadd_rn(tot, __ldcg(ws + (size_t)s * BD + i));
+        constexpr int kMax = 2 * kF32MaxD / kF32Slab;  // 32 slabs at most
+        float part[kMax];
+#pragma unroll
+        for (int s = 0; s < kMax; ++s) part[s] = s < nslab ? __ldcg(ws + (size_t)s * BD + i) : 0.0f;
+        float tot = part[0];
+#pragma unroll
+        for (int s = 1; s < kMax; ++s)
+            if (s < nslab) tot = __fadd_rn(tot, part[s]);
         const double x = (double)temb[i];
         const double sg = 1.0 / (1.0 + exp(-x));
         d_temb[i] = (float)((double)tot * (sg * (1.0 + x * (1.0 - sg))));
@@ -418,9 +422,16 @@ cudaError_t launch_f32_out_fwd(const float *x, const float *emb, float *out, flo
     if (cps < 1) cps = 1;
     const int rows = (S + cps - 1) / cps;
     const dim3 grid((unsigned)((S + rows - 1) / rows), (unsigned)B);
-    cudaError_t err = ensure_smem_attr((const void *)f32_out_fwd_kernel, smem, dev);
+    if (D / 4 <= 32 * 24) {  // D <= 3072: 24 vectors per lane, two CTAs per SM
+        cudaError_t err = ensure_smem_attr((const void *)f32_out_fwd_kernel<24>, smem, dev);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(f32_out_fwd_kernel<24>, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D, eps,
+                          rows);
+    }
+    cudaError_t err = ensure_smem_attr((const void *)f32_out_fwd_kernel<kF32FwdVPL>, smem, dev);
     if (err != cudaSuccess) return err;
-    return launch_pdl(f32_out_fwd_kernel, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D, eps, rows);
+    return launch_pdl(f32_out_fwd_kernel<kF32FwdVPL>, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D,
+                      eps, rows);
 }
 
 cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
@@ -431,9 +442,19 @@ cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb
     const int H = 2 * D;
     float *sig = static_cast<float *>(ws);
     float *kap = sig + (size_t)B * T * H;
-    const int nt = (D / 4 + 31) / 32 * 32;
-    cudaError_t err = launch_pdl(f32_out_bwd_tile_kernel, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
-                                 emb, mean, rstd, dx, sig, kap, S, D, T);
+    // two CTAs per SM: two vectors (8 columns) per thread up to D = 3072 (at most
+    // 384 threads), four up to D = 4096 (at most 256)
+    const int V = D / 4;
+    cudaError_t err;
+    if (V <= 768) {
+        const int nt = ((V + 1) / 2 + 31) / 32 * 32;
+        err = launch_pdl(f32_out_bwd_tile_kernel<2>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb,
+                         mean, rstd, dx, sig, kap, S, D, T);
+    } else {
+        const int nt = ((V + 3) / 4 + 31) / 32 * 32;
+        err = launch_pdl(f32_out_bwd_tile_kernel<4>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb,
+                         mean, rstd, dx, sig, kap, S, D, T);
+    }
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
 }

@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(MAXNT, MINB)
 out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
                     const uint16_t *__restrict__ emb, const float *__restrict__ mean,
                     const float *__restrict__ rstd, uint16_t *__restrict__ dx, float *__restrict__ ws_sig,
-                    float *__restrict__ ws_kap, int S, int D, int T) {
+                    float *__restrict__ ws_kap, int S, int D, int T, int keep_dx) {
     static_assert((RB == 1 || RB == 2 || RB == 4) && NST >= 2 * RB && NST <= kBwdMaxStages && NST % RB == 0,
                   "whole blocks of rows per stage group, two blocks in flight");
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -642,8 +642,10 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
         const int v = tid + NT * j;
         sc_v[j] = (EXACT || v < V) ? ldg16(e + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // dy and dx are streamed once: evict-first in L2
+    // dy and dx are streamed once: evict-first in L2 (dx evict-last when a
+    // following kernel of the same call reads it)
     const uint64_t pol_stream = l2_evict_first();
+    const uint64_t pol_dx = keep_dx ? l2_evict_last() : pol_stream;
     if (tid == 0) {
         for (int i = 0; i < NST && i < n; ++i) {
             unsigned char *dst = stages + (size_t)i * stage_bytes;
@@ -734,7 +736,7 @@ out_bwd_tile_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict_
                     const px2 t = px_fma(px_bf16(xa[q]), nk2, k3v);
                     o[q] = px_to_bf16x2(px_fma(gh, rs2, t));
                 }
-                stg16_hint(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_stream);
+                stg16_hint(drow + (size_t)v * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_dx);
             }
         }
     };
@@ -1066,7 +1068,7 @@ cudaError_t launch_zero(float *p, size_t n, cudaStream_t stream) {
 template <int VPT, int MAXNT, int MINB, int RB, int NST>
 static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                                     const float *rstd, uint16_t *dx, float *sig, float *kap, int B, int S, int D,
-                                    int T, cudaStream_t stream, const DeviceInfo &dev) {
+                                    int T, cudaStream_t stream, const DeviceInfo &dev, bool keep_dx) {
     const int V = D / 8;
     const int nt = ((V + VPT - 1) / VPT + 31) / 32 * 32;
     const size_t smem = ((sizeof(BwdSmem) + 127) / 128) * 128 + (size_t)NST * 4 * D;
@@ -1076,7 +1078,7 @@ static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(T, B), dim3(nt), smem, stream, dy, x, emb, mean, rstd, dx, sig, kap,
-                      S, D, T);
+                      S, D, T, keep_dx ? 1 : 0);
 }
 
 // 16 columns per thread.  Stages of up to 12 KB (D <= 3072): two CTAs of <= 192
@@ -1085,7 +1087,7 @@ static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const
 // 2 rows and 4 stages (at most 128 KB).
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
-                           cudaStream_t stream, const DeviceInfo &dev) {
+                           cudaStream_t stream, const DeviceInfo &dev, bool keep_dx) {
     if (S == 0) return launch_zero(d_emb, (size_t)B * 2 * D, stream);
     const int T = (S + kTile - 1) / kTile;
     const int H = 2 * D;
@@ -1094,11 +1096,11 @@ cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t
     const int V = D / 8;
     cudaError_t err;
     if (V <= 384)
-        err = launch_out_bwd_t<2, 192, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<2, 192, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
     else if (V <= 512)
-        err = launch_out_bwd_t<2, 256, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<2, 256, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
     else
-        err = launch_out_bwd_t<4, 256, 1, 2, 4>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev);
+        err = launch_out_bwd_t<4, 256, 1, 2, 4>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
 }

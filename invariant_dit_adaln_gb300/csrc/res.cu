@@ -154,7 +154,8 @@ cudaError_t launch_res_bwd(const uint16_t *d_out, const uint16_t *d_r, const uin
                            uint16_t *d_x, uint16_t *d_residual, float *d_emb, float *d_gate, void *ws, int B, int S,
                            int D, cudaStream_t stream, const DeviceInfo &dev) {
     // the LayerNorm + modulation backward at r: dr_ln into d_residual, d_emb
-    cudaError_t err = launch_out_bwd(d_out, r, emb, mean, rstd, d_residual, d_emb, ws, B, S, D, stream, dev);
+    // dr_ln stays in L2 for the tail kernel
+    cudaError_t err = launch_out_bwd(d_out, r, emb, mean, rstd, d_residual, d_emb, ws, B, S, D, stream, dev, true);
     if (err != cudaSuccess) return err;
     if (S == 0) return launch_zero(d_gate, (size_t)B * D, stream);
     const int T = (S + kTile - 1) / kTile;
