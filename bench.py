@@ -42,9 +42,11 @@ FLUSH_BYTES = 512 << 20
 # forward, backward tile, tree fold, projection-backward slab, d_temb
 KERNELS_PER_STEP = 7
 # DRAM bytes (read + write) of one adaln_out_bwd call (tile kernel + tree fold)
-# at this workload, from one ncu capture of the current kernels (dram__bytes_read.sum
-# + dram__bytes_write.sum); None when the kernels changed after the capture.
-OUT_BWD_DRAM_BYTES = None
+# at this workload, from one ncu capture of the current kernels
+# (dram__bytes_read.sum + dram__bytes_write.sum of both kernels, mean of two
+# calls; dx lines still in L2 when a replayed launch ends are not counted).
+# None when the kernels change after the capture.
+OUT_BWD_DRAM_BYTES = 117_004_800
 
 
 # ---------------------------------------------------------------------------
