@@ -477,7 +477,8 @@ adaln_status adaln_scale_residual_norm_bwd(const adaln_bf16 *d_out, const adaln_
  * a word instead of hanging, the kernel lets the copies it issued land, and it
  * returns without finishing its outputs.  Codes: 0x101 adaln_out_fwd, 0x201
  * adaln_out_bwd, 0x301 and 0x302 adaln_proj_fwd (CUDA-core and tensor-core
- * kernels), 0x303 adaln_out_fwd_proj; bit 0x8000 is or-ed in when an issued
+ * kernels), 0x303 adaln_out_fwd_proj (the first code found, LayerNorm kernels
+ * first, when several kernels failed); bit 0x8000 is or-ed in when an issued
  * copy did not land within the limit while the kernel was leaving.  Returns 0
  * when no kernel failed, -1 if a word could not be read.
  *

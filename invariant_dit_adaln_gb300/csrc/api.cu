@@ -481,12 +481,15 @@ adaln_status adaln_proj_wgrad_rows(const float *d_emb, const adaln_bf16 *u, int 
 
 int adaln_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    // the LayerNorm kernels' word first, then the projection kernels'; all cleared
+    // the first kernel code of the LayerNorm kernels' word, then the projection
+    // kernels' words; the drain bit of any word; all words cleared
     const int a = read_and_clear_device_error();
     const int b = read_and_clear_proj_error();
     const int c = read_and_clear_tc_error();
     if (a < 0 || b < 0 || c < 0) return -1;
-    return a != 0 ? a : b != 0 ? b : c;
+    const int drain = (a | b | c) & (int)kErrDrainFailed;
+    const int ca = a & ~(int)kErrDrainFailed, cb = b & ~(int)kErrDrainFailed, cc = c & ~(int)kErrDrainFailed;
+    return (ca != 0 ? ca : cb != 0 ? cb : cc) | drain;
 }
 
 }  // extern "C"

@@ -453,6 +453,9 @@ struct PoSmem {
     uint32_t tmem;
     int abort;
     int bad;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+    uint64_t never;  // test builds: a barrier nothing arrives on
+#endif
 };
 
 __global__ void __launch_bounds__(128, 1)
@@ -481,6 +484,9 @@ proj_out_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         mbar_init(&sm.done, 1);
         sm.abort = 0;
         sm.bad = 0;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+        mbar_init(&sm.never, 1);
+#endif
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -538,6 +544,13 @@ proj_out_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         // ---- MMA issuer ----
         for (int i = 0; i < nst; ++i) {
             const int st = i % kPoStages;
+#ifdef ADALN_TEST_WAIT_NEVER_NS
+            // test builds: the first wait runs out of time
+            if (i == 0 && !mbar_wait_bounded(&sm.never, 0u, (uint64_t)(ADALN_TEST_WAIT_NEVER_NS))) {
+                *abort_flag = 1;
+                break;
+            }
+#endif
             if (!mbar_wait_or_abort(&sm.full[st], (uint32_t)(i / kPoStages) & 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;
