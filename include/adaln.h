@@ -24,7 +24,9 @@
  *    buffer has zero bytes (B == 0 or S == 0), and for the optional outputs
  *    marked "or NULL".  bf16 tensors are passed as their 16-bit
  *    patterns (adaln_bf16); all tensors are dense, row-major, no strides.
- *  - The caller owns every buffer, including workspaces.  The library never
+ *  - The caller owns every buffer, including workspaces.  A workspace's
+ *    contents on entry do not matter (no call needs it zeroed) and are
+ *    undefined on return.  The library never
  *    allocates, never frees and never synchronizes: work is enqueued on
  *    `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
  *    returns at once.  Kernels may be launched with programmatic dependent
