@@ -379,10 +379,19 @@ f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restric
 __global__ void __launch_bounds__(256)
 f32_proj_bwd_final_kernel(const float *__restrict__ ws, const float *__restrict__ temb, float *__restrict__ d_temb,
                           int B, int D, int nslab) {
-    pdl_wait();
-    pdl_trigger();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
+    // silu'(t) in fp64 before the wait (temb is an input of this call; the
+    // kernel before this one is the call's own slab kernel, which cannot write
+    // it, and which started only after all earlier work had completed)
+    double dsl = 0.0;
+    if (i < BD) {
+        const double x = (double)temb[i];
+        const double sg = 1.0 / (1.0 + exp(-x));
+        dsl = sg * (1.0 + x * (1.0 - sg));
+    }
+    pdl_wait();
+    pdl_trigger();
     if (i < BD) {
         constexpr int kMax = 2 * kF32MaxD / kF32Slab;  // 32 slabs at most
         float part[kMax];
@@ -392,9 +401,7 @@ f32_proj_bwd_final_kernel(const float *__restrict__ ws, const float *__restrict_
 #pragma unroll
         for (int s = 1; s < kMax; ++s)
             if (s < nslab) tot = __fadd_rn(tot, part[s]);
-        const double x = (double)temb[i];
-        const double sg = 1.0 / (1.0 + exp(-x));
-        d_temb[i] = (float)((double)tot * (sg * (1.0 + x * (1.0 - sg))));
+        d_temb[i] = (float)((double)tot * dsl);
     }
 }
 

@@ -608,12 +608,16 @@ constexpr int kMaxSlabs = 2 * kMaxD / kProjSlabRows;  // 64
 __global__ void __launch_bounds__(256)
 proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__ temb, uint16_t *__restrict__ d_temb,
                       int B, int D, int nslab) {
-    pdl_wait();
-    pdl_trigger();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long BD = (long long)B * D;
+    // silu'(t) before the wait: temb is an input of this call, the kernels
+    // before this one are the call's own (they cannot write temb: outputs
+    // never overlap inputs), and the call's first kernel let this one start
+    // only after its own wait, i.e. after all earlier work had completed
+    const float ds = i < BD ? dsilu_f32(bf16f(temb[i])) : 0.0f;
+    pdl_wait();
+    pdl_trigger();
     if (i < BD) {
-        const float ds = dsilu_f32(bf16f(temb[i]));
         float tot;
         if (nslab == 24) {
             // D = 3072: all 24 partials requested before the first add
