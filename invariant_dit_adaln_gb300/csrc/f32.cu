@@ -107,9 +107,10 @@ f32_proj_fwd_kernel(const float *__restrict__ u, const float *__restrict__ W, co
 // LayerNorm + modulation forward: one warp per token row, rows of one sample
 // per CTA (onep and shift of the sample in shared memory).  Lane l holds the
 // float4 vectors l, l + 32, ... of the row in registers (D <= 4096).  Sums:
-// per lane in vector order, the four elements in order, then the xor
-// butterfly; mean = sum / D, var = sum (x - mean)^2 / D, rstd = 1 / sqrt(var
-// + eps), each operation rounded once.
+// per lane in vector order, even and odd columns in the two halves of a packed
+// accumulator (packed fp32x2 instructions, explicit rounding), the halves
+// added, then the xor butterfly; mean = sum / D, var = sum (x - mean)^2 / D,
+// rstd = 1 / sqrt(var + eps), each operation rounded once.
 // --------------------------------------------------------------------------
 constexpr int kF32FwdVPL = kF32MaxD / 128;  // 32 vectors per lane at most
 
@@ -144,38 +145,41 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
             const int v = lane + 32 * j;
             xv[j] = v < V ? ldf4_hint(xr + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        float s1 = 0.0f;
+        // sums by column pair (packed), the halves added, then the butterfly
+        px2 s1 = 0ull;
 #pragma unroll
         for (int j = 0; j < VPL; ++j)
             if (lane + 32 * j < V)
-                s1 = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s1, xv[j].x), xv[j].y), xv[j].z), xv[j].w);
-        const float mu = __fdiv_rn(warp_sum(s1), Df);
-        auto sq = [&](float a, float acc) {
-            const float d = __fsub_rn(a, mu);
-            return __fadd_rn(acc, __fmul_rn(d, d));
-        };
-        float s2 = 0.0f;
+                s1 = px_add(px_add(s1, px_make(xv[j].x, xv[j].y)), px_make(xv[j].z, xv[j].w));
+        const float mu = __fdiv_rn(warp_sum(__fadd_rn(px_lo(s1), px_hi(s1))), Df);
+        const px2 mu2 = px_splat(mu);
+        px2 s2 = 0ull;
 #pragma unroll
         for (int j = 0; j < VPL; ++j)
-            if (lane + 32 * j < V) s2 = sq(xv[j].w, sq(xv[j].z, sq(xv[j].y, sq(xv[j].x, s2))));
-        const float var = __fdiv_rn(warp_sum(s2), Df);
+            if (lane + 32 * j < V) {
+                const px2 d0 = px_sub(px_make(xv[j].x, xv[j].y), mu2);
+                const px2 d1 = px_sub(px_make(xv[j].z, xv[j].w), mu2);
+                s2 = px_add(px_add(s2, px_mul(d0, d0)), px_mul(d1, d1));
+            }
+        const float var = __fdiv_rn(warp_sum(__fadd_rn(px_lo(s2), px_hi(s2))), Df);
         const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+        const px2 rs2 = px_splat(rs);
         if (lane == 0) {
             mean[row] = mu;
             rstd[row] = rs;
         }
         float4 *orow = reinterpret_cast<float4 *>(out + row * D);
-        auto mod = [&](float a, float on, float sh) {
-            return __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(a, mu), rs), on), sh);
+        // out = fp32(fp32(fp32(fp32(x - mean) * rstd) * onep) + shift)
+        auto mod = [&](float a, float b, float on_a, float on_b, float sh_a, float sh_b) {
+            return px_add(px_mul(px_mul(px_sub(px_make(a, b), mu2), rs2), px_make(on_a, on_b)), px_make(sh_a, sh_b));
         };
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
             if (v < V) {
                 const float4 a = xv[j], on = po[v], sh = ps[v];
-                stg16f_hint(orow + v, make_float4(mod(a.x, on.x, sh.x), mod(a.y, on.y, sh.y), mod(a.z, on.z, sh.z),
-                                                  mod(a.w, on.w, sh.w)),
-                            pol);
+                const px2 lo = mod(a.x, a.y, on.x, on.y, sh.x, sh.y), hi = mod(a.z, a.w, on.z, on.w, sh.z, sh.w);
+                stg16f_hint(orow + v, make_float4(px_lo(lo), px_hi(lo), px_lo(hi), px_hi(hi)), pol);
             }
         }
     }
@@ -187,9 +191,12 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
 // (j < VPT: two per thread up to D = 3072, four up to 4096).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
 // p = fp32(g * xhat) and g go into the columns' tiles by TwoSum from (+0, +0);
 // each thread's fused multiply-add sums of g * onep and p * onep over its
-// columns, the warp butterfly, the warps in ascending order: c1, c2 (divided
-// by D); dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(xhat * c2))).  Two CTAs
-// per SM hide the loads' latency.
+// columns (even and odd columns in the two halves of a packed accumulator,
+// then added), the warp butterfly, the warps in ascending order: c1, c2
+// (divided by D); dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(xhat * c2))).
+// All arithmetic on column pairs in packed fp32x2 instructions with explicit
+// rounding (a float4 of a row is two pairs as loaded).  Two CTAs per SM hide
+// the loads' latency.
 // --------------------------------------------------------------------------
 template <int VPT>
 __global__ void __launch_bounds__(VPT == 2 ? 384 : 256, 2)
@@ -208,80 +215,85 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
     const int H = 2 * D;
     pdl_wait();
     pdl_trigger();
-    float4 onep[VPT];
+    // onep = fp32(1 + scale) of this thread's columns, by column pair
+    px2 onep[VPT][2];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
-        if (v < V) {
-            const float4 sc = reinterpret_cast<const float4 *>(emb + (size_t)b * 2 * D)[v];
-            onep[j] = make_float4(__fadd_rn(1.0f, sc.x), __fadd_rn(1.0f, sc.y), __fadd_rn(1.0f, sc.z),
-                                  __fadd_rn(1.0f, sc.w));
-        } else {
-            onep[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        }
+        float4 sc = make_float4(-1.0f, -1.0f, -1.0f, -1.0f);
+        if (v < V) sc = reinterpret_cast<const float4 *>(emb + (size_t)b * 2 * D)[v];
+        onep[j][0] = px_make(__fadd_rn(1.0f, sc.x), __fadd_rn(1.0f, sc.y));
+        onep[j][1] = px_make(__fadd_rn(1.0f, sc.z), __fadd_rn(1.0f, sc.w));
     }
-    float ss[VPT][4], ks[VPT][4], sh[VPT][4], kh[VPT][4];
+    // tree nodes of the scale products p and of the shift products g, by
+    // column pair, from (+0, +0)
+    px2 ss[VPT][2], ks[VPT][2], sh[VPT][2], kh[VPT][2];
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ss[j][c] = ks[j][c] = sh[j][c] = kh[j][c] = 0.0f;
+        for (int c = 0; c < 2; ++c) ss[j][c] = ks[j][c] = sh[j][c] = kh[j][c] = 0ull;
     const int s0 = t * kTile;
     const int n = min(kTile, S - s0);
     const float Df = (float)D;
     const uint64_t pol = l2_evict_first();
-    auto load = [&](int i, float4 (&xa)[VPT], float4 (&ga)[VPT]) {
+    for (int i = 0; i < n; ++i) {
         const size_t row = (size_t)b * S + s0 + i;
+        px2 xp[VPT][2], gp[VPT][2];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = tid + NT * j;
-            xa[j] = v < V ? ldf4_hint(x + row * D + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            ga[j] = v < V ? ldf4_hint(dy + row * D + (size_t)v * 4, pol) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            uint4 xw = make_uint4(0u, 0u, 0u, 0u), gw = xw;
+            if (v < V) {
+                xw = ldg16_hint(x + row * D + (size_t)v * 4, pol);
+                gw = ldg16_hint(dy + row * D + (size_t)v * 4, pol);
+            }
+            xp[j][0] = px_make(__uint_as_float(xw.x), __uint_as_float(xw.y));
+            xp[j][1] = px_make(__uint_as_float(xw.z), __uint_as_float(xw.w));
+            gp[j][0] = px_make(__uint_as_float(gw.x), __uint_as_float(gw.y));
+            gp[j][1] = px_make(__uint_as_float(gw.z), __uint_as_float(gw.w));
         }
-    };
-    for (int i = 0; i < n; ++i) {
-        float4 xc[VPT], gc[VPT];
-        load(i, xc, gc);
-        const size_t row = (size_t)b * S + s0 + i;
         const float mu = mean[row], rs = rstd[row];
-        float a1 = 0.0f, a2 = 0.0f;
-        float xh[VPT][4];
+        const px2 mu2 = px_splat(mu), rs2 = px_splat(rs);
+        // phase 1: x_hat, the tree products and this thread's row sums (column
+        // pairs in packed fused multiply-adds, the halves added at the end)
+        px2 a1 = 0ull, a2 = 0ull;
+        px2 xh[VPT][2];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             if (tid + NT * j < V) {
-                const float xe[4] = {xc[j].x, xc[j].y, xc[j].z, xc[j].w};
-                const float ge[4] = {gc[j].x, gc[j].y, gc[j].z, gc[j].w};
-                const float oe[4] = {onep[j].x, onep[j].y, onep[j].z, onep[j].w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    xh[j][c] = __fmul_rn(__fsub_rn(xe[c], mu), rs);
-                    const float p = __fmul_rn(ge[c], xh[j][c]);
-                    twosum(ss[j][c], ks[j][c], p);
-                    twosum(sh[j][c], kh[j][c], ge[c]);
-                    a1 = __fmaf_rn(ge[c], oe[c], a1);
-                    a2 = __fmaf_rn(p, oe[c], a2);
+                for (int c = 0; c < 2; ++c) {
+                    xh[j][c] = px_mul(px_sub(xp[j][c], mu2), rs2);
+                    const px2 p = px_mul(gp[j][c], xh[j][c]);
+                    px_twosum(ss[j][c], ks[j][c], p);
+                    px_twosum(sh[j][c], kh[j][c], gp[j][c]);
+                    a1 = px_fma(gp[j][c], onep[j][c], a1);
+                    a2 = px_fma(p, onep[j][c], a2);
                 }
+            } else {
+                xh[j][0] = xh[j][1] = 0ull;
             }
         }
-        a1 = warp_sum(a1);
-        a2 = warp_sum(a2);
-        if (lane == 0) red[i & 1][warp] = make_float2(a1, a2);
+        const float s1 = warp_sum(__fadd_rn(px_lo(a1), px_hi(a1)));
+        const float s2 = warp_sum(__fadd_rn(px_lo(a2), px_hi(a2)));
+        if (lane == 0) red[i & 1][warp] = make_float2(s1, s2);
         __syncthreads();
         float t1 = red[i & 1][0].x, t2 = red[i & 1][0].y;
         for (int w = 1; w < nw; ++w) t1 = __fadd_rn(t1, red[i & 1][w].x), t2 = __fadd_rn(t2, red[i & 1][w].y);
-        const float c1 = __fdiv_rn(t1, Df), c2 = __fdiv_rn(t2, Df);
+        const px2 c1 = px_splat(__fdiv_rn(t1, Df)), c2 = px_splat(__fdiv_rn(t2, Df));
+        // phase 2: dx = fp32(rstd * fp32(fp32(gh - c1) - fp32(x_hat * c2))), gh = fp32(g * onep)
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = tid + NT * j;
             if (v < V) {
-                const float ge[4] = {gc[j].x, gc[j].y, gc[j].z, gc[j].w};
-                const float oe[4] = {onep[j].x, onep[j].y, onep[j].z, onep[j].w};
-                float o[4];
+                px2 o[2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float gh = __fmul_rn(ge[c], oe[c]);
-                    o[c] = __fmul_rn(rs, __fsub_rn(__fsub_rn(gh, c1), __fmul_rn(xh[j][c], c2)));
+                for (int c = 0; c < 2; ++c) {
+                    const px2 gh = px_mul(gp[j][c], onep[j][c]);
+                    o[c] = px_mul(rs2, px_sub(px_sub(gh, c1), px_mul(xh[j][c], c2)));
                 }
-                stg16f_hint(dx + row * D + (size_t)v * 4, make_float4(o[0], o[1], o[2], o[3]), pol);
+                stg16f_hint(dx + row * D + (size_t)v * 4, make_float4(px_lo(o[0]), px_hi(o[0]), px_lo(o[1]), px_hi(o[1])),
+                            pol);
             }
         }
         // red[i & 1] is written again two rows later, after the next barrier
@@ -291,10 +303,10 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
         const int v = tid + NT * j;
         if (v < V) {
             const size_t node = ((size_t)b * T + t) * H + (size_t)v * 4;
-            stg16f(ws_sig + node, make_float4(ss[j][0], ss[j][1], ss[j][2], ss[j][3]));
-            stg16f(ws_kap + node, make_float4(ks[j][0], ks[j][1], ks[j][2], ks[j][3]));
-            stg16f(ws_sig + node + D, make_float4(sh[j][0], sh[j][1], sh[j][2], sh[j][3]));
-            stg16f(ws_kap + node + D, make_float4(kh[j][0], kh[j][1], kh[j][2], kh[j][3]));
+            stg16f(ws_sig + node, make_float4(px_lo(ss[j][0]), px_hi(ss[j][0]), px_lo(ss[j][1]), px_hi(ss[j][1])));
+            stg16f(ws_kap + node, make_float4(px_lo(ks[j][0]), px_hi(ks[j][0]), px_lo(ks[j][1]), px_hi(ks[j][1])));
+            stg16f(ws_sig + node + D, make_float4(px_lo(sh[j][0]), px_hi(sh[j][0]), px_lo(sh[j][1]), px_hi(sh[j][1])));
+            stg16f(ws_kap + node + D, make_float4(px_lo(kh[j][0]), px_hi(kh[j][0]), px_lo(kh[j][1]), px_hi(kh[j][1])));
         }
     }
 }
