@@ -51,6 +51,9 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
 
 // a packed bf16x2 word as (lo, hi) floats: exact
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+// eager bf16 multiply and add of two bf16 values: the fp32 result rounded once
+__device__ __forceinline__ float eager_mul(float a, float b) { return bf16f(bf16_bits(__fmul_rn(a, b))); }
+__device__ __forceinline__ float eager_add(float a, float b) { return bf16f(bf16_bits(__fadd_rn(a, b))); }
 
 // --------------------------------------------------------------------------
 // packed fp32x2 arithmetic (one instruction for two lanes of work on sm_103a),

@@ -58,6 +58,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean, float *rstd,
                            int B, int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev,
                            bool keep_out = false);
+// the block-level norm's forward fused into the LayerNorm kernel (D <= 4096)
+bool out_fwd_res_supported(int D);
+cudaError_t launch_out_fwd_res(const uint16_t *x, const uint16_t *residual, const uint16_t *gate,
+                               const uint16_t *emb, uint16_t *r, uint16_t *out, float *mean, float *rstd, int B,
+                               int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev);
 // keep_dx: write dx as evict-last in L2 (a following kernel reads it)
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,

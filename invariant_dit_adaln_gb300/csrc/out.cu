@@ -288,22 +288,26 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
 // column pairs of a vector in order; the two accumulators, then the two halves
 // of the pairs; then a fixed xor butterfly.  It depends on D only.
 // ==========================================================================
-template <int VPL, int MAXW>
+template <int VPL, int MAXW, bool RES>
 __global__ void __launch_bounds__(MAXW * 32, 1)
 out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
                    float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int cps, int NS,
-                   int keep_out) {
+                   int keep_out, const uint16_t *__restrict__ residual, const uint16_t *__restrict__ gate,
+                   uint16_t *__restrict__ r_out) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int NW = blockDim.x >> 5;
     const int V = D >> 3;
     const int row_bytes = D * 2;
+    // a stage holds the x row, and with RES the residual row after it
+    const int stage_bytes = RES ? 2 * row_bytes : row_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);             // [warps][NS] (+ 1: test builds)
     float *t_onep = reinterpret_cast<float *>(smem_raw + 1024);          // [D]
     float *t_shift = t_onep + D;                                         // [D]
-    unsigned char *ring = smem_raw + 1024 + (size_t)D * 8;               // [warps][NS][row]
-    unsigned char *my_ring = ring + (size_t)warp * NS * row_bytes;
+    uint4 *t_gate = reinterpret_cast<uint4 *>(smem_raw + 1024 + (size_t)D * 8);  // RES: the sample's gate, [V]
+    unsigned char *ring = smem_raw + 1024 + (size_t)D * (RES ? 10 : 8);  // [warps][NS][stage]
+    unsigned char *my_ring = ring + (size_t)warp * NS * stage_bytes;
     uint64_t *my_full = full + warp * NS;
 
     const int b = blockIdx.x / cps;
@@ -332,9 +336,13 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     }
     if (lane == 0)
         for (int k = 0; k < NS && k < nrows; ++k) {
-            mbar_arrive_expect_tx(&my_full[k], row_bytes);
-            bulk_g2s(my_ring + (size_t)k * row_bytes, x + (row0 + (size_t)k * NW) * D, row_bytes, &my_full[k]);
+            unsigned char *dst = my_ring + (size_t)k * stage_bytes;
+            mbar_arrive_expect_tx(&my_full[k], stage_bytes);
+            bulk_g2s(dst, x + (row0 + (size_t)k * NW) * D, row_bytes, &my_full[k]);
+            if (RES) bulk_g2s(dst + row_bytes, residual + (row0 + (size_t)k * NW) * D, row_bytes, &my_full[k]);
         }
+    if (RES)
+        for (int i = threadIdx.x; i < V; i += blockDim.x) t_gate[i] = ldg16(gate + (size_t)b * D + (size_t)i * 8);
     // the sample's modulation parameters, fp32
     for (int i = threadIdx.x; i < V; i += blockDim.x) {
         const uint4 sc = i == (int)threadIdx.x ? sc0 : ldg16(e + (size_t)i * 8);
@@ -364,6 +372,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     const float Df = (float)D;
     // out is not read again by this operator, unless a fused projection reads it next
     const uint64_t pol_out = keep_out ? l2_evict_last() : l2_evict_first();
+    const uint64_t pol_r = l2_evict_first();
     for (int k = 0; k < nrows; ++k) {
         const size_t r = row0 + (size_t)k * NW;
         const int st = k % NS;
@@ -382,17 +391,40 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
             }
             return;
         }
-        const uint4 *srow = reinterpret_cast<const uint4 *>(my_ring + (size_t)st * row_bytes);
+        const uint4 *srow = reinterpret_cast<const uint4 *>(my_ring + (size_t)st * stage_bytes);
         uint4 xr[VPL];
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
             xr[j] = v < V ? srow[v] : make_uint4(0u, 0u, 0u, 0u);
+            if (RES && v < V) {
+                // the gated residual, in eager bf16: r = bf16(residual + bf16(gate * x)); r is normalised below
+                const uint4 rv = srow[V + v], gv = t_gate[v];
+                const uint32_t xa[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w}, ra[4] = {rv.x, rv.y, rv.z, rv.w},
+                               ga[4] = {gv.x, gv.y, gv.z, gv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o[q] = pack_bf16x2(eager_add(bf16lo(ra[q]), eager_mul(bf16lo(ga[q]), bf16lo(xa[q]))),
+                                       eager_add(bf16hi(ra[q]), eager_mul(bf16hi(ga[q]), bf16hi(xa[q]))));
+                xr[j] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
         __syncwarp();  // every lane has its part of the row: refill the stage
         if (lane == 0 && k + NS < nrows) {
-            mbar_arrive_expect_tx(&my_full[st], row_bytes);
-            bulk_g2s(my_ring + (size_t)st * row_bytes, x + (r + (size_t)NS * NW) * D, row_bytes, &my_full[st]);
+            unsigned char *dst = my_ring + (size_t)st * stage_bytes;
+            mbar_arrive_expect_tx(&my_full[st], stage_bytes);
+            bulk_g2s(dst, x + (r + (size_t)NS * NW) * D, row_bytes, &my_full[st]);
+            if (RES) bulk_g2s(dst + row_bytes, residual + (r + (size_t)NS * NW) * D, row_bytes, &my_full[st]);
+        }
+        if (RES) {
+            // r is read again only by the backward: streamed out
+            uint16_t *rrow = r_out + r * D;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                const int v = lane + 32 * j;
+                if (v < V) stg16_hint(rrow + (size_t)v * 8, xr[j], pol_r);
+            }
         }
         // mean (zero vectors past the row end add +0 and change nothing)
         float2 s1[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
@@ -456,17 +488,28 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
     }
 }
 
-template <int VPL, int MAXW>
+template <int VPL, int MAXW, bool RES = false>
 static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, uint16_t *out, float *mean,
                                       float *rstd, int B, int S, int D, float eps, cudaStream_t stream,
-                                      const DeviceInfo &dev, bool keep_out) {
+                                      const DeviceInfo &dev, bool keep_out, const uint16_t *residual = nullptr,
+                                      const uint16_t *gate = nullptr, uint16_t *r_out = nullptr) {
     constexpr size_t kSmemMax = 227 * 1024;
-    auto smem_of = [&](int warps, int ns) { return 1024 + (size_t)D * 8 + (size_t)warps * ns * D * 2; };
-    // 16 warps with 2 stages each where that fits, else 8 warps with 3 (or 2)
-    int warps = 8, ns = smem_of(8, 3) <= kSmemMax ? 3 : 2;
-    if (MAXW == 16 && smem_of(16, 2) <= kSmemMax) { warps = 16; ns = 2; }
+    const size_t stage = (size_t)D * 2 * (RES ? 2 : 1);
+    auto smem_of = [&](int warps, int ns) { return 1024 + (size_t)D * (RES ? 10 : 8) + (size_t)warps * ns * stage; };
+    int warps, ns;
+    if (!RES) {
+        // 16 warps with 2 stages each where that fits, else 8 warps with 3 (or 2)
+        warps = 8;
+        ns = smem_of(8, 3) <= kSmemMax ? 3 : 2;
+        if (MAXW == 16 && smem_of(16, 2) <= kSmemMax) { warps = 16; ns = 2; }
+    } else {
+        // two rows per stage: all the warps with 2 stages, else with 1
+        warps = MAXW;
+        ns = smem_of(MAXW, 2) <= kSmemMax ? 2 : 1;
+        if (smem_of(warps, ns) > kSmemMax) warps = 8;
+    }
     const size_t smem = smem_of(warps, ns);
-    auto kern = out_fwd_row_kernel<VPL, MAXW>;
+    auto kern = out_fwd_row_kernel<VPL, MAXW, RES>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     // about one CTA per SM in all; every CTA within one sample
@@ -475,7 +518,7 @@ static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, ui
     if (cps < 1) cps = 1;
     const long long grid = (long long)B * cps;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(warps * 32), smem, stream, x, emb, out, mean, rstd, S, D, eps,
-                      cps, ns, keep_out ? 1 : 0);
+                      cps, ns, keep_out ? 1 : 0, residual, gate, r_out);
 }
 
 template <int VPT, int BLK, int NST, int MINB>
@@ -517,6 +560,28 @@ cudaError_t launch_out_fwd(const uint16_t *x, const uint16_t *emb, uint16_t *out
         case 5: case 6: return launch_out_fwd_t<6, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
         default: return launch_out_fwd_t<8, 2, 4, 1>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, keep_out);
     }
+}
+
+// The block-level norm's forward in one kernel (rows of up to 8 KB): r =
+// bf16(residual + bf16(gate * x)) is formed from staged x and residual rows,
+// written, and normalised and modulated in registers, so r is never read back.
+bool out_fwd_res_supported(int D) { return D / 8 <= 512; }
+
+cudaError_t launch_out_fwd_res(const uint16_t *x, const uint16_t *residual, const uint16_t *gate,
+                               const uint16_t *emb, uint16_t *r, uint16_t *out, float *mean, float *rstd, int B,
+                               int S, int D, float eps, cudaStream_t stream, const DeviceInfo &dev) {
+    const int V = D / 8;
+    if (V <= 128)
+        return launch_out_fwd_row<4, 16, true>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, false, residual,
+                                               gate, r);
+    if (V <= 256)
+        return launch_out_fwd_row<8, 16, true>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, false, residual,
+                                               gate, r);
+    if (V <= 384)
+        return launch_out_fwd_row<12, 16, true>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, false, residual,
+                                                gate, r);
+    return launch_out_fwd_row<16, 8, true>(x, emb, out, mean, rstd, B, S, D, eps, stream, dev, false, residual, gate,
+                                           r);
 }
 
 // ==========================================================================

@@ -21,10 +21,6 @@
 
 namespace adaln {
 
-// eager bf16 multiply and add of two bf16 values: the fp32 result rounded once
-__device__ __forceinline__ float eager_mul(float a, float b) { return bf16f(bf16_bits(__fmul_rn(a, b))); }
-__device__ __forceinline__ float eager_add(float a, float b) { return bf16f(bf16_bits(__fadd_rn(a, b))); }
-
 // --------------------------------------------------------------------------
 // forward: r = bf16(residual + bf16(gate * x)), 8 elements per thread and
 // step, grid-stride; r keeps the default L2 policy, because the LayerNorm
@@ -143,6 +139,8 @@ cudaError_t launch_res_fwd(const uint16_t *x, const uint16_t *residual, const ui
     long long grid = (n8 + 255) / 256;
     const long long cap = (long long)dev.sm_count * 8;
     if (grid > cap) grid = cap;
+    if (out_fwd_res_supported(D))  // one kernel: r is formed, written and normalised in registers
+        return launch_out_fwd_res(x, residual, gate, emb, r, out, mean, rstd, B, S, D, eps, stream, dev);
     cudaError_t err = launch_pdl(res_add_kernel, dim3((unsigned)grid), dim3(256), 0, stream, x, residual, gate, r,
                                  n8, S, D);
     if (err != cudaSuccess) return err;

@@ -4,7 +4,8 @@ Kernels that wait on their own bulk copies give each wait a time limit; a wait
 that runs out sets the library's device error word and the kernel drains the
 copies it issued, then returns.  A test build of the library sends the first
 wait of every waiting kernel to an mbarrier that nothing ever arrives on (a
-200 us limit), so the path runs: the forward reports 0x101, the backward 0x201,
+200 us limit), so the path runs: the forward (also the block-level norm's)
+reports 0x101, the backward 0x201,
 the tensor-core projection 0x302 and proj_out 0x303 (the MMA thread gives up,
 the TMA thread stops and lets its copies land, the cluster writes nothing and
 frees its tensor memory), no drain runs out (the 0x8000 bit stays clear), and the GPU context
@@ -36,6 +37,7 @@ def wait_lib():
     L.adaln_out_bwd.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_size_t, I, I, I, P]
     L.adaln_proj_fwd.argtypes = [P, P, P, P, P, I, I, P]
     L.adaln_out_fwd_proj.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, ctypes.c_float, P]
+    L.adaln_scale_residual_norm_fwd.argtypes = [P] * 8 + [I, I, I, ctypes.c_float, P]
     L.adaln_device_error.restype = I
     return L
 
@@ -82,6 +84,14 @@ def test_waits_that_run_out_report_and_return(wait_lib, B, S, D):
     y = torch.empty((B, S, 64), dtype=torch.bfloat16, device="cuda")
     assert L.adaln_out_fwd_proj(inp["x"].data_ptr(), emb.data_ptr(), Wp.data_ptr(), bp.data_ptr(), out.data_ptr(),
                                 mean.data_ptr(), rstd.data_ptr(), y.data_ptr(), B, S, D, 64, 1e-6, st) == 0
+    err = L.adaln_device_error()
+    assert err & ~DRAIN_FAILED == FWD_WAIT and not err & DRAIN_FAILED, hex(err)
+    # the block-level norm's forward (the gated residual formed in the LayerNorm kernel where D <= 4096)
+    gate = torch.zeros((B, D), dtype=torch.bfloat16, device="cuda")
+    r = torch.empty_like(inp["x"])
+    assert L.adaln_scale_residual_norm_fwd(inp["x"].data_ptr(), inp["dy"].data_ptr(), gate.data_ptr(), emb.data_ptr(),
+                                           r.data_ptr(), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(), B, S, D,
+                                           1e-6, st) == 0
     err = L.adaln_device_error()
     assert err & ~DRAIN_FAILED == FWD_WAIT and not err & DRAIN_FAILED, hex(err)
     assert L.adaln_device_error() == 0  # read and cleared
