@@ -992,7 +992,7 @@ def run_block(args, rank, local):
                       "value": B * S / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
                       "algorithmic_bytes_per_step": alg, "hbm_gbs": alg / (ms / 1e3) / 1e9,
                       "hbm_frac": alg / (ms / 1e3) / 1e9 / peak, "peak_gbs": peak, "peak_source": peak_src,
-                      "kernels_per_step": 6, "steps_per_pass": K, "passes": len(passes),
+                      "kernels_per_step": 5, "steps_per_pass": K, "passes": len(passes),
                       "l2": "two input sets alternate (each: four 50.3 MB token inputs and four 50.3 MB token outputs, more than L2); no flush",
                       "data": "synthetic (seeded, drawn on the device)"}), flush=True)
 
