@@ -46,7 +46,7 @@ KERNELS_PER_STEP = 7
 # (dram__bytes_read.sum + dram__bytes_write.sum of both kernels, mean of two
 # calls; dx lines still in L2 when a replayed launch ends are not counted).
 # None when the kernels change after the capture.
-OUT_BWD_DRAM_BYTES = 117_004_800
+OUT_BWD_DRAM_BYTES = 116_796_288
 
 
 # ---------------------------------------------------------------------------
