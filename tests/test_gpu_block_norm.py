@@ -86,8 +86,12 @@ def _check_case(i, with_dr=True):
 
 @pytest.mark.parametrize("B,S,D,seed,outl", [(2, 33, 3072, 0, 0.0), (1, 1, 3072, 1, 0.0), (2, 69, 3072, 2, 0.03),
                                              (3, 7, 256, 3, 0.0), (2, 40, 8, 4, 0.0), (1, 35, 4104, 5, 0.0),
-                                             (2, 1100, 64, 6, 0.0)])
+                                             (2, 1100, 64, 6, 0.0), (2, 50, 2048, 10, 0.0), (1, 40, 4096, 11, 0.02),
+                                             (2, 600, 3072, 12, 0.0)])
 def test_scale_residual_norm(B, S, D, seed, outl):
+    """The forward forms r inside the LayerNorm kernel up to D = 4096 (16 warps
+    with one or two stages, or 8 warps at D = 4096; at S = 600 some warps of a
+    CTA have no row) and with a separate gated-add kernel beyond (D = 4104)."""
     _check_case(synth.make_block_inputs(B, S, D, seed, outlier_frac=outl))
 
 
