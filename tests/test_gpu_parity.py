@@ -104,7 +104,8 @@ def test_proj_fwd_weight_zero_gives_bias():
 
 @pytest.mark.parametrize("B,S,D,seed,outl", [(2, 33, 3072, 0, 0.0), (2, 64, 3072, 1, 0.05), (1, 1, 3072, 2, 0.0),
                                              (3, 7, 256, 3, 0.0), (2, 5, 8, 4, 0.0), (2, 9, 520, 5, 0.0),
-                                             (1, 3, 8192, 6, 0.0), (2, 6, 4104, 7, 0.2)])
+                                             (1, 3, 8192, 6, 0.0), (2, 6, 4104, 7, 0.2), (2, 9, 2056, 8, 0.0),
+                                             (1, 5, 4096, 9, 0.0)])
 def test_out_fwd(B, S, D, seed, outl):
     inp = synth.make_inputs(B, S, D, seed, outlier_frac=outl)
     emb = synth.normal_bf16(synth.stream_key(seed, "aux"), B * 2 * D, std=0.3).reshape(B, 2 * D)
@@ -140,7 +141,9 @@ def test_out_fwd_plain_layernorm_and_constant_rows():
 
 @pytest.mark.parametrize("B,S,D,seed,outl", [(2, 33, 3072, 0, 0.0), (1, 1, 3072, 1, 0.0), (2, 32, 3072, 2, 0.0),
                                              (2, 69, 3072, 3, 0.03), (3, 7, 256, 4, 0.0), (2, 40, 8, 5, 0.0),
-                                             (1, 35, 4104, 6, 0.0), (1, 33, 8192, 7, 0.0), (1, 1100, 64, 8, 0.0)])
+                                             (1, 35, 4104, 6, 0.0), (1, 33, 8192, 7, 0.0), (1, 1100, 64, 8, 0.0),
+                                             (2, 45, 2056, 9, 0.0), (2, 40, 2560, 10, 0.02), (2, 33, 2048, 11, 0.0),
+                                             (1, 37, 4096, 12, 0.0)])
 def test_out_bwd(B, S, D, seed, outl):
     inp = synth.make_inputs(B, S, D, seed, outlier_frac=outl)
     emb = synth.normal_bf16(synth.stream_key(seed, "aux"), B * 2 * D, std=0.3).reshape(B, 2 * D)
