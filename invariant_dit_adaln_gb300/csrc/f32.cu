@@ -188,7 +188,7 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
 // --------------------------------------------------------------------------
 // LayerNorm + modulation backward and the level-0 tree tiles: one CTA per
 // (sample b, 32-token tile t); thread i owns the float4 vectors i + NT j
-// (j < VPT: two per thread up to D = 3072, four up to 4096).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
+// (j < VPT: three per thread up to D = 3072, four up to 4096).  Per row in ascending s: xhat = fp32(fp32(x - mean) * rstd), g = dy,
 // p = fp32(g * xhat) and g go into the columns' tiles by TwoSum from (+0, +0);
 // each thread's fused multiply-add sums of g * onep and p * onep over its
 // columns (even and odd columns in the two halves of a packed accumulator,
@@ -198,8 +198,8 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
 // rounding (a float4 of a row is two pairs as loaded).  Two CTAs per SM hide
 // the loads' latency.
 // --------------------------------------------------------------------------
-template <int VPT>
-__global__ void __launch_bounds__(VPT == 2 ? 384 : 256, 2)
+template <int VPT, int MAXNT>
+__global__ void __launch_bounds__(MAXNT, 2)
 f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ x, const float *__restrict__ emb,
                         const float *__restrict__ mean, const float *__restrict__ rstd, float *__restrict__ dx,
                         float *__restrict__ ws_sig, float *__restrict__ ws_kap, int S, int D, int T) {
@@ -461,18 +461,19 @@ cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb
     const int H = 2 * D;
     float *sig = static_cast<float *>(ws);
     float *kap = sig + (size_t)B * T * H;
-    // two CTAs per SM: two vectors (8 columns) per thread up to D = 3072 (at most
-    // 384 threads), four up to D = 4096 (at most 256)
+    // two CTAs per SM: three vectors (12 columns: more independent TwoSum
+    // chains per thread) per thread up to D = 3072 (at most 256 threads), four
+    // up to D = 4096 (at most 256)
     const int V = D / 4;
     cudaError_t err;
     if (V <= 768) {
-        const int nt = ((V + 1) / 2 + 31) / 32 * 32;
-        err = launch_pdl(f32_out_bwd_tile_kernel<2>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb,
-                         mean, rstd, dx, sig, kap, S, D, T);
+        const int nt = ((V + 2) / 3 + 31) / 32 * 32;
+        err = launch_pdl(f32_out_bwd_tile_kernel<3, 256>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
+                         emb, mean, rstd, dx, sig, kap, S, D, T);
     } else {
         const int nt = ((V + 3) / 4 + 31) / 32 * 32;
-        err = launch_pdl(f32_out_bwd_tile_kernel<4>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb,
-                         mean, rstd, dx, sig, kap, S, D, T);
+        err = launch_pdl(f32_out_bwd_tile_kernel<4, 256>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
+                         emb, mean, rstd, dx, sig, kap, S, D, T);
     }
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
