@@ -46,7 +46,7 @@ KERNELS_PER_STEP = 7
 # (dram__bytes_read.sum + dram__bytes_write.sum of both kernels, mean of two
 # calls; dx lines still in L2 when a replayed launch ends are not counted).
 # None when the kernels change after the capture.
-OUT_BWD_DRAM_BYTES = 116_796_288
+OUT_BWD_DRAM_BYTES = 117_004_800
 
 
 # ---------------------------------------------------------------------------
@@ -547,10 +547,11 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     eager_ms = statistics.median(a.elapsed_time(c) for a, c in eg)
 
-    # ---- per-call pass: events around each call (roofline of the dominant call) ----
+    # ---- per-call pass: each call timed alone, L2 flushed before it (roofline of the dominant call) ----
     K2 = min(K, 300)
     names = ["adaln_proj_fwd", "adaln_out_fwd", "adaln_out_bwd", "adaln_proj_bwd"]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K2)]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+          for _ in range(K2)]
     calls = [
         lambda: binding.adaln_proj_fwd(temb, W, b, emb=emb, u=u, stream=stream),
         lambda: binding.adaln_out_fwd(x, emb, out=out, mean=mean, rstd=rstd, stream=stream),
@@ -559,13 +560,13 @@ def run_gpu(args, world, rank, local):
                                        stream=stream),
     ]
     for i in range(K2):
-        flush()
-        ev[i][0].record(stream)
         for j, c in enumerate(calls):
+            flush()
+            ev[i][j][0].record(stream)
             c()
-            ev[i][j + 1].record(stream)
+            ev[i][j][1].record(stream)
     torch.cuda.synchronize()
-    call_ms = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K2)) for j, n in enumerate(names)}
+    call_ms = {n: statistics.mean(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K2)) for j, n in enumerate(names)}
 
     # ---- end to end: host buffers in, host buffers out, every step ----
     K3 = min(K, 100)

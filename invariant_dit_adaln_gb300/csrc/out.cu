@@ -1146,13 +1146,10 @@ static cudaError_t launch_out_bwd_t(const uint16_t *dy, const uint16_t *x, const
                       S, D, T, keep_dx ? 1 : 0);
 }
 
-// Stages of up to 8 KB (D <= 2048): 16 columns per thread, two CTAs of <= 128
-// threads per SM, blocks of 4 rows, 8 stages; up to 12 KB (D <= 3072): 24
-// columns per thread (24 independent TwoSum chains: more work in flight per
-// warp, which this latency-bound kernel gains from), two CTAs of <= 128
-// threads per SM, the same ring; up to 16 KB: 16 columns per thread, one CTA of
-// <= 256 threads per SM; longer rows: 32 columns per thread, blocks of 2 rows
-// and 4 stages (at most 128 KB).
+// 16 columns per thread.  Stages of up to 12 KB (D <= 3072): two CTAs of <= 192
+// threads per SM, blocks of 4 rows, 8 stages; up to 16 KB: one CTA of <= 256
+// threads per SM, the same ring; longer rows: 32 columns per thread, blocks of
+// 2 rows and 4 stages (at most 128 KB).
 cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t *emb, const float *mean,
                            const float *rstd, uint16_t *dx, float *d_emb, void *ws, int B, int S, int D,
                            cudaStream_t stream, const DeviceInfo &dev, bool keep_dx) {
@@ -1163,10 +1160,8 @@ cudaError_t launch_out_bwd(const uint16_t *dy, const uint16_t *x, const uint16_t
     float *kap = sig + (size_t)B * T * H;
     const int V = D / 8;
     cudaError_t err;
-    if (V <= 256)
+    if (V <= 384)
         err = launch_out_bwd_t<2, 192, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
-    else if (V <= 384)
-        err = launch_out_bwd_t<3, 128, 2, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
     else if (V <= 512)
         err = launch_out_bwd_t<2, 256, 1, 4, 8>(dy, x, emb, mean, rstd, dx, sig, kap, B, S, D, T, stream, dev, keep_dx);
     else
