@@ -442,7 +442,11 @@ struct SlabSmem {
 //   kSlabDsOnly   nothing (dW and db come from the tiled kernels)
 //   kSlabDwOut    dW and db in bf16, overwrite, no fp32 accumulators
 //   kSlabGeneral  any of dW_acc, db_acc (accumulate or overwrite), dW, db
-constexpr int kSlabDsOnly = 0, kSlabDwOut = 1, kSlabGeneral = 2;
+//   kSlabDwFull   kSlabDwOut where every slab is whole (D % 256 == 0, so every
+//                 warp has 32 rows and every lane's columns lie inside D) and
+//                 the chunk holds all BC samples: no per-row tests, row
+//                 pointers stepped by a fixed stride, db after the rows
+constexpr int kSlabDsOnly = 0, kSlabDwOut = 1, kSlabGeneral = 2, kSlabDwFull = 3;
 
 template <int BC, int WM>
 __global__ void __launch_bounds__(256, 2)
@@ -570,13 +574,64 @@ proj_bwd_slab_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
                 }
             }
         };
-        load_batch(wa, 0);
-        load_batch(wb, kPre);
-        for (int i0 = 0; i0 < cnt; i0 += 2 * kPre) {
-            use_batch(wa, i0);
-            if (i0 + 2 * kPre < cnt) load_batch(wa, i0 + 2 * kPre);
-            use_batch(wb, i0 + kPre);
-            if (i0 + 3 * kPre < cnt) load_batch(wb, i0 + 3 * kPre);
+        // kSlabDwFull: the same arithmetic in the same order as kSlabDwOut
+        if constexpr (WM == kSlabDwFull) {
+            const size_t step = (size_t)8 * D;  // from one of this warp's rows to the next
+            const uint16_t *wrow = W + (size_t)(n0 + warp) * D + col;
+            uint16_t *drow = dW + (size_t)(n0 + warp) * D + col;
+            auto fload = [&](uint4(&wv)[kPre], int i0) {
+#pragma unroll
+                for (int p = 0; p < kPre; ++p) wv[p] = ldg16(wrow + (size_t)(i0 + p) * step);
+            };
+            auto fuse = [&](const uint4(&wv)[kPre], int i0) {
+#pragma unroll
+                for (int p = 0; p < kPre; ++p) {
+                    const int r = warp + 8 * (i0 + p);
+                    const float2 w2[4] = {bf16x2_to_f2(wv[p].x), bf16x2_to_f2(wv[p].y), bf16x2_to_f2(wv[p].z),
+                                          bf16x2_to_f2(wv[p].w)};
+                    float2 acc[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int b = 0; b < BC; ++b) {
+                        const float2 e2 = f2splat(sm.es[b][r]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            ds[b][q] = f2fma(e2, w2[q], ds[b][q]);
+                            acc[q] = f2fma(e2, uf[b][q], acc[q]);
+                        }
+                    }
+                    stg16_hint(drow + (size_t)(i0 + p) * step,
+                               make_uint4(pack_bf16x2(acc[0].x, acc[0].y), pack_bf16x2(acc[1].x, acc[1].y),
+                                          pack_bf16x2(acc[2].x, acc[2].y), pack_bf16x2(acc[3].x, acc[3].y)),
+                               pol_dw);
+                }
+            };
+            fload(wa, 0);
+            fload(wb, kPre);
+#pragma unroll
+            for (int i0 = 0; i0 < kRowsPerWarp; i0 += 2 * kPre) {
+                fuse(wa, i0);
+                if (i0 + 2 * kPre < kRowsPerWarp) fload(wa, i0 + 2 * kPre);
+                fuse(wb, i0 + kPre);
+                if (i0 + 3 * kPre < kRowsPerWarp) fload(wb, i0 + 3 * kPre);
+            }
+            // db of the slab's rows: samples in ascending order from +0, one thread per row
+            if (kchunk == 0)
+                for (int rr = threadIdx.x; rr < kSlabRows; rr += blockDim.x) {
+                    float a = 0.0f;
+                    for (int b = 0; b < nb; ++b) a = __fadd_rn(a, sm.es[b][rr]);
+                    db[n0 + rr] = bf16_bits(a);
+                }
+        } else {
+            load_batch(wa, 0);
+            load_batch(wb, kPre);
+            for (int i0 = 0; i0 < cnt; i0 += 2 * kPre) {
+                use_batch(wa, i0);
+                if (i0 + 2 * kPre < cnt) load_batch(wa, i0 + 2 * kPre);
+                use_batch(wb, i0 + kPre);
+                if (i0 + 3 * kPre < cnt) load_batch(wb, i0 + 3 * kPre);
+            }
         }
         // the slab's partial d_silu: warps added in ascending order
 #pragma unroll
@@ -841,8 +896,12 @@ static cudaError_t launch_slab_w(const float *d_emb, const uint16_t *u, const ui
                                  float *db_acc, uint16_t *dW, uint16_t *db, int accumulate, float *ws, int B, int D,
                                  cudaStream_t stream, const DeviceInfo &dev) {
     // dW and db both wanted in bf16, nothing accumulated: the branch-free form
-    if (!dW_acc && !db_acc && !accumulate && dW && db)
+    if (!dW_acc && !db_acc && !accumulate && dW && db) {
+        if (D % kProjKChunk == 0 && B == BC)
+            return launch_slab<BC, kSlabDwFull>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream,
+                                                dev);
         return launch_slab<BC, kSlabDwOut>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
+    }
     return launch_slab<BC, kSlabGeneral>(d_emb, u, W, dW_acc, db_acc, dW, db, accumulate, ws, B, D, stream, dev);
 }
 
