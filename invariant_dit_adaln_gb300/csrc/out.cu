@@ -288,7 +288,8 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
 // column pairs of a vector in order; the two accumulators, then the two halves
 // of the pairs; then a fixed xor butterfly.  It depends on D only.
 // ==========================================================================
-template <int VPL, int MAXW, bool RES>
+// EXACT: V == 32 * VPL, every lane's vectors lie inside the row (no tests)
+template <int VPL, int MAXW, bool RES, bool EXACT>
 __global__ void __launch_bounds__(MAXW * 32, 1)
 out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb, uint16_t *__restrict__ out,
                    float *__restrict__ mean, float *__restrict__ rstd, int S, int D, float eps, int cps, int NS,
@@ -396,8 +397,8 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
-            xr[j] = v < V ? srow[v] : make_uint4(0u, 0u, 0u, 0u);
-            if (RES && v < V) {
+            xr[j] = (EXACT || v < V) ? srow[v] : make_uint4(0u, 0u, 0u, 0u);
+            if (RES && (EXACT || v < V)) {
                 // the gated residual, in eager bf16: r = bf16(residual + bf16(gate * x)); r is normalised below
                 const uint4 rv = srow[V + v], gv = t_gate[v];
                 const uint32_t xa[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w}, ra[4] = {rv.x, rv.y, rv.z, rv.w},
@@ -423,7 +424,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
 #pragma unroll
             for (int j = 0; j < VPL; ++j) {
                 const int v = lane + 32 * j;
-                if (v < V) stg16_hint(rrow + (size_t)v * 8, xr[j], pol_r);
+                if (EXACT || v < V) stg16_hint(rrow + (size_t)v * 8, xr[j], pol_r);
             }
         }
         // mean (zero vectors past the row end add +0 and change nothing)
@@ -442,7 +443,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
         float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
-            if (lane + 32 * j < V) {
+            if (EXACT || lane + 32 * j < V) {
                 const uint32_t wa[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -460,7 +461,7 @@ out_fwd_row_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ 
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = lane + 32 * j;
-            if (v < V) {
+            if (EXACT || v < V) {
                 const float4 *po = reinterpret_cast<const float4 *>(t_onep);
                 const float4 *ps = reinterpret_cast<const float4 *>(t_shift);
                 const float4 oa = po[v], ob = po[V + v], sa = ps[v], sb = ps[V + v];
@@ -509,7 +510,7 @@ static cudaError_t launch_out_fwd_row(const uint16_t *x, const uint16_t *emb, ui
         if (smem_of(warps, ns) > kSmemMax) warps = 8;
     }
     const size_t smem = smem_of(warps, ns);
-    auto kern = out_fwd_row_kernel<VPL, MAXW, RES>;
+    auto kern = D / 8 == 32 * VPL ? out_fwd_row_kernel<VPL, MAXW, RES, true> : out_fwd_row_kernel<VPL, MAXW, RES, false>;
     cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
     // about one CTA per SM in all; every CTA within one sample
