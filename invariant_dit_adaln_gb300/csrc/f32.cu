@@ -312,28 +312,46 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
 }
 
 // --------------------------------------------------------------------------
-// Projection backward: one CTA per (256 columns, 256-row slab of W), thread =
-// column k.  Over the slab's rows n ascending: d_silu partials
-// ds[b] = fma(e[b,n], W[n,k], ds[b]) (written per slab: ws[slab][b][k]), and
-// the weight gradient acc = fma(e[b,n], u[b,k], acc) over the samples
-// ascending, starting from the accumulator (accumulate) or +0; db likewise
-// with additions.  Samples in chunks of kF32BC; a later chunk continues from
-// the accumulator the earlier one wrote.
+// Projection backward: one CTA per (256 columns, 256-row slab of W).  A thread
+// owns 4 consecutive columns (one float4 of every row) and one of 4 row groups
+// of the slab (rows rg, rg + 4, ...).  Over its rows ascending: d_silu partials
+// ds[b] = fma(e[b,n], W[n,k], ds[b]); the slab's partial is the four groups'
+// added in ascending group order (written per slab: ws[slab][b][k]).  The
+// weight gradient acc = fma(e[b,n], u[b,k], acc) over the samples ascending,
+// starting from the accumulator (accumulate) or +0; db likewise with
+// additions.  Samples in chunks of kF32BC; a later chunk continues from the
+// accumulator the earlier one wrote.  All orders depend on D only.
 // --------------------------------------------------------------------------
 constexpr int kF32Slab = 256;
-constexpr int kF32SlabRowsInFlight = 32;  // rows of W each thread has requested at once
+constexpr int kF32RowGroups = 4;
+constexpr int kF32SlabRowsInFlight = 8;  // rows of W (a float4 each) each thread has requested at once
 
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ float4 ldf4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 fma4(float a, float4 b, float4 c) {
+    return make_float4(__fmaf_rn(a, b.x, c.x), __fmaf_rn(a, b.y, c.y), __fmaf_rn(a, b.z, c.z),
+                       __fmaf_rn(a, b.w, c.w));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+__global__ void __launch_bounds__(256, 2)
 f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restrict__ u, const float *__restrict__ W,
                          float *__restrict__ dW_acc, float *__restrict__ db_acc, int accumulate,
                          float *__restrict__ ws, int B, int D) {
     __shared__ float es[kF32BC][kF32Slab];
-    const int k = blockIdx.x * 256 + threadIdx.x;
+    __shared__ float4 part[kF32RowGroups - 1][kF32BC][64];  // row groups 1..3's partials
+    const int ct = threadIdx.x & 63;
+    const int rg = threadIdx.x >> 6;
+    const int k = blockIdx.x * 256 + ct * 4;  // the first of this thread's 4 columns
     const int slab = blockIdx.y;
     const int N = 2 * D;
     const int n0 = slab * kF32Slab;
     const int rows = min(kF32Slab, N - n0);
-    const bool live = k < D;
+    const int nrow = rows > rg ? (rows - rg + kF32RowGroups - 1) / kF32RowGroups : 0;  // rows of this group
+    const bool live = k < D;  // D % 4 == 0: all 4 columns inside D
     pdl_wait();
     pdl_trigger();
     for (int b0 = 0; b0 < B; b0 += kF32BC) {
@@ -344,46 +362,61 @@ f32_proj_bwd_slab_kernel(const float *__restrict__ d_emb, const float *__restric
             es[bb][r] = (bb < nb && r < rows) ? d_emb[(size_t)(b0 + bb) * N + n0 + r] : 0.0f;
         }
         __syncthreads();
-        float uk[kF32BC], ds[kF32BC];
+        float4 uk[kF32BC], ds[kF32BC];
 #pragma unroll
         for (int bb = 0; bb < kF32BC; ++bb) {
-            uk[bb] = (live && bb < nb) ? u[(size_t)(b0 + bb) * D + k] : 0.0f;
-            ds[bb] = 0.0f;
+            uk[bb] = (live && bb < nb) ? ldf4(u + (size_t)(b0 + bb) * D + k) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            ds[bb] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         const bool first = b0 == 0 && !accumulate;
-        for (int r0 = 0; r0 < rows; r0 += kF32SlabRowsInFlight) {
-            float w[kF32SlabRowsInFlight];  // requested before the first use
+        const float *wcol = W + (size_t)(n0 + rg) * D + k;
+        float *acol = dW_acc ? dW_acc + (size_t)(n0 + rg) * D + k : nullptr;
+        const size_t step = (size_t)kF32RowGroups * D;  // from one row of the group to the next
+        for (int i0 = 0; i0 < nrow; i0 += kF32SlabRowsInFlight) {
+            float4 w[kF32SlabRowsInFlight];  // requested before the first use
 #pragma unroll
             for (int q = 0; q < kF32SlabRowsInFlight; ++q)
-                w[q] = (live && r0 + q < rows) ? __ldg(W + (size_t)(n0 + r0 + q) * D + k) : 0.0f;
+                w[q] = (live && i0 + q < nrow) ? ldf4(wcol + (size_t)(i0 + q) * step)
+                                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
             for (int q = 0; q < kF32SlabRowsInFlight; ++q) {
-                const int r = r0 + q;
-                if (r < rows) {
+                const int i = i0 + q;
+                if (i < nrow) {
+                    const int r = rg + kF32RowGroups * i;
 #pragma unroll
                     for (int bb = 0; bb < kF32BC; ++bb)
-                        if (bb < nb) ds[bb] = __fmaf_rn(es[bb][r], w[q], ds[bb]);
-                    if (dW_acc && live) {
-                        float *pa = dW_acc + (size_t)(n0 + r) * D + k;
-                        float a = first ? 0.0f : *pa;
+                        if (bb < nb) ds[bb] = fma4(es[bb][r], w[q], ds[bb]);
+                    if (acol && live) {
+                        float4 *pa = reinterpret_cast<float4 *>(acol + (size_t)i * step);
+                        float4 a = first ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *pa;
 #pragma unroll
                         for (int bb = 0; bb < kF32BC; ++bb)
-                            if (bb < nb) a = __fmaf_rn(es[bb][r], uk[bb], a);
+                            if (bb < nb) a = fma4(es[bb][r], uk[bb], a);
                         *pa = a;
                     }
                 }
             }
         }
+        // the slab's partial: row groups added in ascending order
+        if (rg > 0)
+#pragma unroll
+            for (int bb = 0; bb < kF32BC; ++bb) part[rg - 1][bb][ct] = ds[bb];
+        __syncthreads();
+        if (rg == 0 && live)
+#pragma unroll
+            for (int bb = 0; bb < kF32BC; ++bb)
+                if (bb < nb) {
+                    float4 t = ds[bb];
+#pragma unroll
+                    for (int g = 1; g < kF32RowGroups; ++g) t = add4(t, part[g - 1][bb][ct]);
+                    __stcg(reinterpret_cast<float4 *>(ws + ((size_t)slab * B + b0 + bb) * D + k), t);
+                }
         if (db_acc && blockIdx.x == 0)
             for (int r = threadIdx.x; r < rows; r += blockDim.x) {
                 float a = first ? 0.0f : db_acc[n0 + r];
                 for (int bb = 0; bb < nb; ++bb) a = __fadd_rn(a, es[bb][r]);
                 db_acc[n0 + r] = a;
             }
-        if (live)
-#pragma unroll
-            for (int bb = 0; bb < kF32BC; ++bb)
-                if (bb < nb) __stcg(ws + ((size_t)slab * B + b0 + bb) * D + k, ds[bb]);
     }
 }
 
