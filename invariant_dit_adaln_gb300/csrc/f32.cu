@@ -198,7 +198,8 @@ f32_out_fwd_kernel(const float *__restrict__ x, const float *__restrict__ emb, f
 // rounding (a float4 of a row is two pairs as loaded).  Two CTAs per SM hide
 // the loads' latency.
 // --------------------------------------------------------------------------
-template <int VPT, int MAXNT>
+// EXACT: D / 4 == blockDim.x * VPT, every thread's vectors inside the row (no tests)
+template <int VPT, int MAXNT, bool EXACT>
 __global__ void __launch_bounds__(MAXNT, 2)
 f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ x, const float *__restrict__ emb,
                         const float *__restrict__ mean, const float *__restrict__ rstd, float *__restrict__ dx,
@@ -221,7 +222,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
         float4 sc = make_float4(-1.0f, -1.0f, -1.0f, -1.0f);
-        if (v < V) sc = reinterpret_cast<const float4 *>(emb + (size_t)b * 2 * D)[v];
+        if (EXACT || v < V) sc = reinterpret_cast<const float4 *>(emb + (size_t)b * 2 * D)[v];
         onep[j][0] = px_make(__fadd_rn(1.0f, sc.x), __fadd_rn(1.0f, sc.y));
         onep[j][1] = px_make(__fadd_rn(1.0f, sc.z), __fadd_rn(1.0f, sc.w));
     }
@@ -243,7 +244,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
         for (int j = 0; j < VPT; ++j) {
             const int v = tid + NT * j;
             uint4 xw = make_uint4(0u, 0u, 0u, 0u), gw = xw;
-            if (v < V) {
+            if (EXACT || v < V) {
                 xw = ldg16_hint(x + row * D + (size_t)v * 4, pol);
                 gw = ldg16_hint(dy + row * D + (size_t)v * 4, pol);
             }
@@ -260,7 +261,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
         px2 xh[VPT][2];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            if (tid + NT * j < V) {
+            if (EXACT || tid + NT * j < V) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     xh[j][c] = px_mul(px_sub(xp[j][c], mu2), rs2);
@@ -285,7 +286,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = tid + NT * j;
-            if (v < V) {
+            if (EXACT || v < V) {
                 px2 o[2];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -301,7 +302,7 @@ f32_out_bwd_tile_kernel(const float *__restrict__ dy, const float *__restrict__ 
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + NT * j;
-        if (v < V) {
+        if (EXACT || v < V) {
             const size_t node = ((size_t)b * T + t) * H + (size_t)v * 4;
             stg16f(ws_sig + node, make_float4(px_lo(ss[j][0]), px_hi(ss[j][0]), px_lo(ss[j][1]), px_hi(ss[j][1])));
             stg16f(ws_kap + node, make_float4(px_lo(ks[j][0]), px_hi(ks[j][0]), px_lo(ks[j][1]), px_hi(ks[j][1])));
@@ -480,10 +481,10 @@ cudaError_t launch_f32_out_fwd(const float *x, const float *emb, float *out, flo
         return launch_pdl(f32_out_fwd_kernel<24>, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D, eps,
                           rows);
     }
-    cudaError_t err = ensure_smem_attr((const void *)f32_out_fwd_kernel<kF32FwdVPL>, smem, dev);
+    auto kern = f32_out_fwd_kernel<kF32FwdVPL>;
+    cudaError_t err = ensure_smem_attr((const void *)kern, smem, dev);
     if (err != cudaSuccess) return err;
-    return launch_pdl(f32_out_fwd_kernel<kF32FwdVPL>, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D,
-                      eps, rows);
+    return launch_pdl(kern, grid, dim3(256), smem, stream, x, emb, out, mean, rstd, S, D, eps, rows);
 }
 
 cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb, const float *mean,
@@ -501,12 +502,14 @@ cudaError_t launch_f32_out_bwd(const float *dy, const float *x, const float *emb
     cudaError_t err;
     if (V <= 768) {
         const int nt = ((V + 2) / 3 + 31) / 32 * 32;
-        err = launch_pdl(f32_out_bwd_tile_kernel<3, 256>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
-                         emb, mean, rstd, dx, sig, kap, S, D, T);
+        auto kern = nt * 3 == V ? f32_out_bwd_tile_kernel<3, 256, true> : f32_out_bwd_tile_kernel<3, 256, false>;
+        err = launch_pdl(kern, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb, mean, rstd, dx, sig,
+                         kap, S, D, T);
     } else {
         const int nt = ((V + 3) / 4 + 31) / 32 * 32;
-        err = launch_pdl(f32_out_bwd_tile_kernel<4, 256>, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x,
-                         emb, mean, rstd, dx, sig, kap, S, D, T);
+        auto kern = f32_out_bwd_tile_kernel<4, 256, false>;  // the exact form spills at 128 registers
+        err = launch_pdl(kern, dim3((unsigned)T, (unsigned)B), dim3(nt), 0, stream, dy, x, emb, mean, rstd, dx, sig,
+                         kap, S, D, T);
     }
     if (err != cudaSuccess) return err;
     return launch_fold(sig, kap, d_emb, B, T, H, stream, dev);
