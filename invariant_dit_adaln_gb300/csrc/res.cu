@@ -58,7 +58,9 @@ res_add_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ resi
 // tokens in ascending order, four rows' loads in flight.  d_residual holds
 // dr_ln on entry (written by the LayerNorm backward) and gr on exit.  The
 // level-0 node of each column is the TwoSum (Neumaier) sum of the tile's
-// products from (+0, +0), as in the LayerNorm backward's tiles.
+// products from (+0, +0), as in the LayerNorm backward's tiles.  Arithmetic on
+// column pairs in packed fp32x2 instructions with explicit rounding; each
+// eager bf16 operation is the fp32 result rounded once (round to nearest even).
 // --------------------------------------------------------------------------
 constexpr int kResRows = 4;
 
@@ -77,16 +79,16 @@ res_gate_bwd_kernel(uint16_t *__restrict__ d_residual, const uint16_t *__restric
     const int s0 = t * kTile;
     const int n = min(kTile, S - s0);
     const size_t base = ((size_t)b * S + s0) * D + (size_t)v * 8;
-    float gf[8];
+    // the sample's gate of this thread's columns, by column pair
+    px2 gf[4];
     {
         const uint4 gv = ldg16(gate + (size_t)b * D + (size_t)v * 8);
-        const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) gf[2 * q] = bf16lo(ga[q]), gf[2 * q + 1] = bf16hi(ga[q]);
+        gf[0] = px_bf16(gv.x), gf[1] = px_bf16(gv.y), gf[2] = px_bf16(gv.z), gf[3] = px_bf16(gv.w);
     }
-    float sg[8], kp[8];
+    // tree nodes of the gate products, by column pair, from (+0, +0)
+    px2 sg[4], kp[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) sg[c] = 0.0f, kp[c] = 0.0f;
+    for (int q = 0; q < 4; ++q) sg[q] = kp[q] = 0ull;
     for (int i0 = 0; i0 < n; i0 += kResRows) {
         uint4 lv[kResRows], dv[kResRows], xv[kResRows];
 #pragma unroll
@@ -108,14 +110,13 @@ res_gate_bwd_kernel(uint16_t *__restrict__ d_residual, const uint16_t *__restric
                 uint32_t go[4], xo[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float gr[2];
-                    gr[0] = d_r ? eager_add(bf16lo(la[q]), bf16lo(da[q])) : bf16lo(la[q]);
-                    gr[1] = d_r ? eager_add(bf16hi(la[q]), bf16hi(da[q])) : bf16hi(la[q]);
-                    const float xx[2] = {bf16lo(xa[q]), bf16hi(xa[q])};
-                    go[q] = pack_bf16x2(gr[0], gr[1]);
-                    xo[q] = pack_bf16x2(__fmul_rn(gr[0], gf[2 * q]), __fmul_rn(gr[1], gf[2 * q + 1]));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) twosum(sg[2 * q + h], kp[2 * q + h], eager_mul(gr[h], xx[h]));
+                    // gr = bf16(dr_ln + d_r) (exact bf16 values, so its store is exact)
+                    const uint32_t grw = d_r ? px_to_bf16x2(px_add(px_bf16(la[q]), px_bf16(da[q]))) : la[q];
+                    const px2 gr = px_bf16(grw);
+                    go[q] = grw;
+                    xo[q] = px_to_bf16x2(px_mul(gr, gf[q]));  // d_x = bf16(gr * gate)
+                    // the tree product bf16(gr * x), by TwoSum
+                    px_twosum(sg[q], kp[q], px_bf16(px_to_bf16x2(px_mul(gr, px_bf16(xa[q])))));
                 }
                 stg16_hint(d_residual + o, make_uint4(go[0], go[1], go[2], go[3]), pol);
                 stg16_hint(d_x + o, make_uint4(xo[0], xo[1], xo[2], xo[3]), pol);
@@ -123,10 +124,10 @@ res_gate_bwd_kernel(uint16_t *__restrict__ d_residual, const uint16_t *__restric
         }
     }
     const size_t node = ((size_t)b * T + t) * D + (size_t)v * 8;
-    stg16f(ws_sig + node, make_float4(sg[0], sg[1], sg[2], sg[3]));
-    stg16f(ws_sig + node + 4, make_float4(sg[4], sg[5], sg[6], sg[7]));
-    stg16f(ws_kap + node, make_float4(kp[0], kp[1], kp[2], kp[3]));
-    stg16f(ws_kap + node + 4, make_float4(kp[4], kp[5], kp[6], kp[7]));
+    stg16f(ws_sig + node, make_float4(px_lo(sg[0]), px_hi(sg[0]), px_lo(sg[1]), px_hi(sg[1])));
+    stg16f(ws_sig + node + 4, make_float4(px_lo(sg[2]), px_hi(sg[2]), px_lo(sg[3]), px_hi(sg[3])));
+    stg16f(ws_kap + node, make_float4(px_lo(kp[0]), px_hi(kp[0]), px_lo(kp[1]), px_hi(kp[1])));
+    stg16f(ws_kap + node + 4, make_float4(px_lo(kp[2]), px_hi(kp[2]), px_lo(kp[3]), px_hi(kp[3])));
 }
 
 // --------------------------------------------------------------------------
