@@ -723,7 +723,7 @@ cudaError_t launch_proj_fwd_tc(const uint16_t *u, const uint16_t *W, const uint1
     };
     int nt, kblk, area, utile;
     if (B <= 8)
-        nt = 1, kblk = 3, area = kTcSmallArea, utile = kTcUTileSmall;
+        nt = 1, kblk = 2, area = kTcSmallArea, utile = kTcUTileSmall;
     else if (tiles_b <= 2)
         nt = tiles_b, kblk = 2, area = kTcSmallArea, utile = kTcUTile;
     else if (tiles_b <= 5)
