@@ -287,6 +287,12 @@ out_fwd_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ emb,
 // lane, vectors j ascending into two packed accumulators (even j, odd j), the
 // column pairs of a vector in order; the two accumulators, then the two halves
 // of the pairs; then a fixed xor butterfly.  It depends on D only.
+//
+// RES (the block-level norm with a gated residual): a stage holds the x row and
+// the residual row, the sample's gate sits in shared memory beside the table,
+// and a lane forms r = bf16(residual + bf16(gate * x)) (eager bf16: each
+// operation's fp32 result rounded once) for its vectors as it takes them from
+// the stage, stores r, and normalises and modulates r as above.
 // ==========================================================================
 // EXACT: V == 32 * VPL, every lane's vectors lie inside the row (no tests)
 template <int VPL, int MAXW, bool RES, bool EXACT>
