@@ -210,8 +210,11 @@ def test_token_sum_tree_output_is_fresh_for_one_token():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("B,D,seed", [(2, 3072, 0), (1, 3072, 1), (4, 3072, 2), (5, 3072, 3), (64, 512, 4),
-                                      (3, 8, 5), (37, 1024, 6), (2, 4104, 7)])
+                                      (3, 8, 5), (37, 1024, 6), (2, 4104, 7), (3, 3072, 8), (1, 256, 9)])
 def test_proj_bwd(B, D, seed):
+    """One pass over W for B <= 4: the whole-slab form where D % 256 == 0 and B
+    fills the sample chunk (B = 1, 2, 4), the general form otherwise (B = 3,
+    D = 8 or 4104); the tiled dW kernels for B > 4."""
     inp = synth.make_inputs(B, 1, D, seed)
     d_emb = (synth.normal(synth.stream_key(seed, "aux"), B * 2 * D) * 4).astype(np.float32).reshape(B, 2 * D)
     temb, W = dev_bf16(inp["temb"]), dev_bf16(inp["W"])
