@@ -697,15 +697,16 @@ proj_bwd_final_kernel(const float *__restrict__ ws, const uint16_t *__restrict__
 }
 
 // --------------------------------------------------------------------------
-// dW / db for many samples: a 64 x 64 tile of dW per CTA, thread (tn, tk)
-// owning rows n0 + 4 tn .. +3 and columns k0 + 4 tk .. +3; samples stream
-// through shared memory 32 at a time and are added in ascending order,
+// dW for many samples: a 128 x 128 tile of dW per CTA, thread (tn, tk) owning
+// rows r0 + 8 tn .. +7 and columns k0 + 8 tk .. +7 (64 accumulators: 64
+// fused multiply-adds per 4 shared-memory loads of a sample); samples stream
+// through shared memory 16 at a time and are added in ascending order,
 // exactly as in the slab kernel: acc = acc + e[b,n] * u[b,k].
 // --------------------------------------------------------------------------
-constexpr int kDwTile = 64;
-constexpr int kDwBChunk = 32;
+constexpr int kDwTile = 128;
+constexpr int kDwBChunk = 16;
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict__ u, float *__restrict__ dW_acc,
                      uint16_t *__restrict__ dW, int accumulate, int B, int D, int n_begin, int nrows) {
     // rows n_begin .. n_begin + nrows - 1 of the gradient; outputs indexed from that first row
@@ -718,13 +719,13 @@ proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
     const int tn = threadIdx.x >> 4;
     pdl_wait();
     pdl_trigger();
-    float acc[4][4];
+    float acc[8][8];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int r = r0 + 4 * tn + a;
+    for (int a = 0; a < 8; ++a) {
+        const int r = r0 + 8 * tn + a;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int k = k0 + 4 * tk + c;
+        for (int c = 0; c < 8; ++c) {
+            const int k = k0 + 8 * tk + c;
             acc[a][c] = (accumulate && r < nrows && k < D) ? dW_acc[(size_t)r * D + k] : 0.0f;
         }
     }
@@ -738,29 +739,32 @@ proj_dw_tiled_kernel(const float *__restrict__ d_emb, const uint16_t *__restrict
         }
         __syncthreads();
         for (int b = 0; b < nb; ++b) {
-            const float4 e4 = *reinterpret_cast<const float4 *>(&es[b][4 * tn]);
-            const float4 u4 = *reinterpret_cast<const float4 *>(&us[b][4 * tk]);
-            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
-            const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
+            const float4 e0 = *reinterpret_cast<const float4 *>(&es[b][8 * tn]);
+            const float4 e1 = *reinterpret_cast<const float4 *>(&es[b][8 * tn + 4]);
+            const float4 u0 = *reinterpret_cast<const float4 *>(&us[b][8 * tk]);
+            const float4 u1 = *reinterpret_cast<const float4 *>(&us[b][8 * tk + 4]);
+            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[a][c] = __fmaf_rn(ev[a], uv[c], acc[a][c]);
+                for (int c = 0; c < 8; ++c) acc[a][c] = __fmaf_rn(ev[a], uv[c], acc[a][c]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int r = r0 + 4 * tn + a;
-        const int k = k0 + 4 * tk;
-        if (r < nrows && k < D) {  // D % 8 == 0, so the 4 columns are all in range
-            if (dW_acc) stg16f(dW_acc + (size_t)r * D + k, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
-            if (dW) {
-                uint2 p;
-                p.x = pack_bf16x2(acc[a][0], acc[a][1]);
-                p.y = pack_bf16x2(acc[a][2], acc[a][3]);
-                *reinterpret_cast<uint2 *>(dW + (size_t)r * D + k) = p;
+    for (int a = 0; a < 8; ++a) {
+        const int r = r0 + 8 * tn + a;
+        const int k = k0 + 8 * tk;
+        if (r < nrows && k < D) {  // D % 8 == 0, so the 8 columns are all in range
+            if (dW_acc) {
+                stg16f(dW_acc + (size_t)r * D + k, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
+                stg16f(dW_acc + (size_t)r * D + k + 4, make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]));
             }
+            if (dW)
+                stg16(dW + (size_t)r * D + k,
+                      make_uint4(pack_bf16x2(acc[a][0], acc[a][1]), pack_bf16x2(acc[a][2], acc[a][3]),
+                                 pack_bf16x2(acc[a][4], acc[a][5]), pack_bf16x2(acc[a][6], acc[a][7])));
         }
     }
 }
